@@ -1,0 +1,469 @@
+"""Benchmark: one decode step of one layer on the LLaMA-13B-shaped batch.
+
+A step is the whole paged decode path for one batch: slot mapping of each
+sequence's new token, the cache write of its K/V rows, paged attention decode
+(partitioned with the log-sum-exp merge where the lengths call for it) and,
+on batches that share prefix blocks, the copy-on-write block copy.  Inputs are
+resident in HBM; the L2 is flushed (a 256 MiB write) before every timed step,
+outside the timed events.
+
+Prints one JSON line.  value = algorithmic bytes of the step / step time (GB/s);
+tokens/s/layer = sequences / step time.  --impl reference times the CPU oracle
+(fp64, the machine's host cores) on a bounded sample of the same batch instead.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload llama13b_b16]
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_293_gb300 import accounting, workloads  # noqa: E402
+
+METRIC = ("paged decode attention HBM GB/s (% of GB300 peak) and decode tokens/s per layer")
+FLUSH_BYTES = 256 << 20
+LENGTH_RECIPES = {
+    "tiny": "fixed {1,17,50,100}",
+    "llama7b": "uniform [128, 2048]",
+    "llama13b_b16": "lognormal median 512 sigma 1, rounded, clipped [16, 4096]",
+    "llama13b_b32": "lognormal median 512 sigma 1, rounded, clipped [16, 4096]",
+    "gqa_prefix": "512 shared + uniform [64, 2048] private",
+    "long_splitk": "uniform [32768, 131072]",
+}
+DEFAULT_WORKLOAD = "llama13b_b16"
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def read_traffic(kernel_file, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it still matches the source."""
+    import hashlib
+    summ = os.path.join(ROOT, "profiles", "decode_%s_traffic.txt" % workload)
+    if not os.path.exists(summ):
+        return None
+    vals = {}
+    with open(summ) as f:
+        for line in f:
+            if ":" in line:
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    h = hashlib.sha256()
+    for name in kernel_file:
+        with open(os.path.join(ROOT, "paged_kv_cache_293_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    if vals.get("source_sha256") != h.hexdigest():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        if self.proc is None or not self.lines:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class Step:
+    """Device buffers and the launch sequence of one decode step through the binding."""
+
+    def __init__(self, P, w, device):
+        self.P, self.w, self.dev = P, w, device
+        i32 = lambda a: torch.as_tensor(np.ascontiguousarray(a, np.int32), device=device)
+        self.bt = i32(w.block_tables)
+        self.pos = i32(w.positions)
+        self.ctx = i32(w.context_lens)
+        self.pairs = i32(w.cow_pairs) if len(w.cow_pairs) else None
+        self.slots = torch.empty(w.num_seqs, dtype=torch.int64, device=device)
+        self.out = torch.empty((w.num_seqs, w.num_q_heads, w.head_dim), dtype=w.q.dtype,
+                               device=device)
+        self.mcl = w.max_context_len
+        self.psize = w.partition_size or P.pkv_choose_partition_size(
+            w.k_pool, w.num_seqs, w.num_q_heads, self.mcl)
+        nbytes = P.pkv_decode_workspace_bytes(w.k_pool, w.num_seqs, w.num_q_heads, self.mcl,
+                                              self.psize)
+        self.ws = P.workspace_tensor(nbytes, device) if nbytes else None
+        self.split = nbytes > 0
+        self.launches = 3 + (1 if self.split else 0) + (1 if self.pairs is not None else 0)
+
+    def pre_decode(self):
+        P, w = self.P, self.w
+        if self.pairs is not None:
+            P.pkv_copy_blocks(w.k_pool, w.v_pool, self.pairs)
+        P.pkv_slot_mapping(self.bt, self.pos, w.block_size, self.slots)
+        P.pkv_kv_cache_write(w.k_pool, w.v_pool, w.k_new, w.v_new, self.slots)
+
+    def decode(self):
+        P, w = self.P, self.w
+        P.pkv_paged_attention_decode(w.q, w.k_pool, w.v_pool, self.bt, self.ctx, w.scale,
+                                     self.out, self.mcl, self.psize, self.ws)
+
+
+def step_bytes(w, psize):
+    e = workloads.ELEM_BYTES[w.dtype]
+    unique = None
+    if len(w.shared_blocks):
+        toks = int(w.context_lens.sum()) - (w.num_seqs - 1) * len(w.shared_blocks) * w.block_size
+        unique = toks
+    dec_logical = accounting.decode_bytes(w.context_lens, w.num_kv_heads, w.num_q_heads,
+                                          w.head_dim, e, e, w.block_size, psize)
+    dec_unique = accounting.decode_bytes(w.context_lens, w.num_kv_heads, w.num_q_heads,
+                                         w.head_dim, e, e, w.block_size, psize,
+                                         unique_tokens=unique)
+    other = accounting.write_bytes(w.num_seqs, w.num_kv_heads, w.head_dim, e) + 12 * w.num_seqs
+    if len(w.cow_pairs):
+        other += accounting.copy_bytes(len(w.cow_pairs), w.num_kv_heads, w.block_size,
+                                       w.head_dim, e)
+    return dec_logical, dec_unique, other
+
+
+def cpu_oracle_rate(w, budget_s=12.0, max_single_s=30.0):
+    """Time the oracle (as it stands) on host copies of a bounded sample of the batch."""
+    import oracle
+    k = workloads.storage_numpy(w.k_pool)
+    v = workloads.storage_numpy(w.v_pool)
+    q = workloads.storage_numpy(w.q)
+    bt, ctx = w.block_tables, w.context_lens
+    # calibrate on the first few sequences, then size the sample
+    n0 = min(4, w.num_seqs)
+    t = time.perf_counter()
+    oracle.paged_decode(w.dtype, k, v, q[:n0], bt[:n0], ctx[:n0], w.scale)
+    per_tok = (time.perf_counter() - t) / max(1, int(ctx[:n0].sum()))
+    n = w.num_seqs
+    while n > 1 and per_tok * int(ctx[:n].sum()) > max_single_s:
+        n //= 2
+    reps, elapsed = 0, 0.0
+    t = time.perf_counter()
+    while elapsed < budget_s or reps == 0:
+        oracle.paged_decode(w.dtype, k, v, q[:n], bt[:n], ctx[:n], w.scale)
+        reps += 1
+        elapsed = time.perf_counter() - t
+        if reps >= 50:
+            break
+    sec = elapsed / reps
+    e = workloads.ELEM_BYTES[w.dtype]
+    b = accounting.decode_bytes(ctx[:n], w.num_kv_heads, w.num_q_heads, w.head_dim, e, e,
+                                w.block_size)
+    return {"gbs": b / sec / 1e9, "tok_s": n / sec, "sec_per_pass": sec, "seqs": n, "reps": reps,
+            "cores": oracle.num_threads()}
+
+
+def run_ours(args):
+    world, rank, local = dist_setup(args.gpus)
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    from paged_kv_cache_293_gb300 import _build
+    if rank == 0:
+        _build.build()
+    barrier(world)
+    from paged_kv_cache_293_gb300 import pagedkv as P
+
+    w = workloads.make(args.workload, seed=args.seed + rank, device=device)
+    st = Step(P, w, device)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        st.pre_decode()
+        st.decode()
+    torch.cuda.synchronize(device)
+    if P.pkv_get_device_error():
+        raise RuntimeError("device error flags set during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(device)
+    with ClockSampler(device.index) as clocks:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            e0, e1, e2 = evs[i]
+            e0.record(stream)
+            st.pre_decode()
+            e1.record(stream)
+            st.decode()
+            e2.record(stream)
+        torch.cuda.synchronize(device)
+        wall = time.perf_counter() - t_wall
+    barrier(world)
+    step_ms = sum(a.elapsed_time(c) for a, _, c in evs) / args.steps
+    dec_ms = sum(b.elapsed_time(c) for _, b, c in evs) / args.steps
+    step_ms_max = max_over_ranks(step_ms, world, device)
+    if P.pkv_get_device_error():
+        raise RuntimeError("device error flags set during the timed steps")
+
+    # end to end through the binding with host buffers: H2D inputs, the step, D2H output
+    e2e = run_e2e(P, w, st, args, device, flush)
+    e2e_ms_max = max_over_ranks(e2e["ms"], world, device)
+
+    dec_logical, dec_unique, other = step_bytes(w, st.psize if st.split else 0)
+    total = dec_logical + other
+    peak, peak_kind = read_peaks()
+    value = world * total / (step_ms_max * 1e-3) / 1e9
+    dec_gbs = dec_unique / (dec_ms * 1e-3) / 1e9
+    traffic = read_traffic(["decode.cuh", "pkv_common.cuh", "kernels_misc.cu"], args.workload)
+
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        r = cpu_oracle_rate(w)
+        cpu = {"value": r["gbs"], "unit": "GB/s", "cores": r["cores"], "kind": "oracle",
+               "tokens_per_s_per_layer": r["tok_s"],
+               "sample": "first %d of %d sequences of the same batch, %d passes, %.2f s per pass, "
+                         "fp64 C with OpenMP" % (r["seqs"], w.num_seqs, r["reps"],
+                                                 r["sec_per_pass"])}
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms_max, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic",
+        "tokens_per_s_per_layer": round(world * w.num_seqs / (step_ms_max * 1e-3), 1),
+        "pct_of_peak": round(100.0 * value / world / peak, 2),
+        "decode_ms": round(dec_ms, 5),
+        "config": {
+            "workload": w.name, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
+            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+            "context_lens": LENGTH_RECIPES.get(args.workload, ""),
+            "mean_context": round(float(w.context_lens.mean()), 1),
+            "max_context": w.max_context_len, "partition_size": st.psize if st.split else 0,
+            "pool_blocks": w.num_blocks,
+            "kv_bytes_per_step": int(w.context_lens.sum()) * accounting.kv_bytes_per_token(
+                w.num_kv_heads, w.head_dim, workloads.ELEM_BYTES[w.dtype]),
+            "l2": "flushed by a 256 MiB write before every timed step (outside the events)",
+            "parallelism": "replicas, one batch per GPU" if world > 1 else "single GPU",
+            "seed": args.seed,
+        },
+        "roofline": {
+            "kernel": "paged_decode_kernel (+ lse_merge_kernel when partitioned)",
+            "bound": "hbm", "achieved": round(dec_gbs, 2), "peak": peak, "unit": "GB/s",
+            "frac": round(dec_gbs / peak, 4), "peak_kind": peak_kind,
+            "traffic": traffic, "algorithmic_bytes": dec_unique,
+        },
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(world * total / (e2e_ms_max * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms_max, 5),
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
+        "gpu_launches": st.launches * args.steps,
+        "clocks": clocks.summary(),
+        "wall_s_timed": round(wall, 3),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(P, w, st, args, device, flush):
+    """Same step, inputs copied from pinned host memory each step and the output read back."""
+    pin = lambda t: t.detach().cpu().pin_memory()
+    h_q, h_k, h_v = pin(w.q), pin(w.k_new), pin(w.v_new)
+    h_bt, h_pos, h_ctx = pin(st.bt), pin(st.pos), pin(st.ctx)
+    h_out = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+    stream = torch.cuda.current_stream(device)
+    pairs = [(h_q, w.q), (h_k, w.k_new), (h_v, w.v_new), (h_bt, st.bt), (h_pos, st.pos),
+             (h_ctx, st.ctx)]
+    h2d = sum(h.numel() * h.element_size() for h, _ in pairs)
+    d2h = h_out.numel() * h_out.element_size()
+    n = max(3, args.steps // 4)
+    times = []
+    for i in range(n + args.warmup):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for h, d in pairs:
+            d.copy_(h, non_blocking=True)
+        st.pre_decode()
+        st.decode()
+        h_out.copy_(st.out, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= args.warmup:
+            times.append(e0.elapsed_time(e1))
+    return {"ms": sum(times) / len(times), "h2d": h2d, "d2h": d2h}
+
+
+def run_reference(args):
+    """The CPU oracle arm: rank 0 only, bounded samples of the same batch on host cores."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    w = workloads.make(args.workload, seed=args.seed, device="cpu")
+    k = workloads.storage_numpy(w.k_pool)
+    v = workloads.storage_numpy(w.v_pool)
+    q = workloads.storage_numpy(w.q)
+    kn, vn = workloads.storage_numpy(w.k_new), workloads.storage_numpy(w.v_new)
+    bt, ctx, pos = w.block_tables, w.context_lens, w.positions
+    # size each step so that warm-up + timed steps take a few minutes at most
+    per_step_budget = max(0.05, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    t = time.perf_counter()
+    oracle.paged_decode(w.dtype, k, v, q[:2], bt[:2], ctx[:2], w.scale)
+    per_tok = (time.perf_counter() - t) / max(1, int(ctx[:2].sum()))
+    n = 1
+    while n < w.num_seqs and per_tok * int(ctx[:n + 1].sum()) <= per_step_budget:
+        n += 1
+
+    def one_step():
+        slots = oracle.slot_mapping(bt[:n], pos[:n], w.block_size)
+        oracle.kv_cache_write(w.dtype, k, v, kn[:n], vn[:n], slots)
+        oracle.paged_decode(w.dtype, k, v, q[:n], bt[:n], ctx[:n], w.scale)
+
+    for _ in range(args.warmup):
+        one_step()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        one_step()
+    sec = (time.perf_counter() - t) / args.steps
+    e = workloads.ELEM_BYTES[w.dtype]
+    b = accounting.decode_bytes(ctx[:n], w.num_kv_heads, w.num_q_heads, w.head_dim, e, e,
+                                w.block_size) + accounting.write_bytes(n, w.num_kv_heads,
+                                                                       w.head_dim, e)
+    value = b / sec / 1e9
+    sample = ("first %d of %d sequences of the %s batch per step (slot mapping, cache write, "
+              "decode), fp64 C with OpenMP" % (n, w.num_seqs, w.name))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sec * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "tokens_per_s_per_layer": round(n / sec, 2),
+        "config": {"workload": w.name, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
+                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                   "block_size": w.block_size,
+                   "context_lens": LENGTH_RECIPES.get(args.workload, ""), "seed": args.seed},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "kind": "oracle",
+                         "cores": oracle.num_threads(), "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

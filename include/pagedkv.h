@@ -1,0 +1,216 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv.so, paged KV-cache decode for GB300 (sm_103a).
+ *
+ * The method: the KV cache of each sequence is cut into fixed-size blocks that
+ * can sit anywhere in GPU memory; a per-sequence block table maps logical
+ * blocks to physical blocks; attention for the new token of a sequence reads
+ * every cached position through that table ("What Is vLLM: The Fast Inference
+ * Engine for Large Language Models", section "How does PagedAttention work?";
+ * "vLLM in Production", section "PagedAttention - Virtual Memory for the KV
+ * Cache"; "Serving models with vLLM", section "How it works: PagedAttention").
+ *
+ * Conventions shared by every entry point:
+ *  - All array arguments are DEVICE pointers to caller-owned memory.  The
+ *    library allocates nothing and keeps no handle to caller memory.
+ *  - stream is a cudaStream_t passed as void*; NULL is the legacy default
+ *    stream.  Every call is asynchronous on that stream and returns after
+ *    enqueueing its kernels; nothing synchronises inside a call (except
+ *    pkv_get_device_error, which says so).
+ *  - Host-checkable argument errors are returned before anything is launched.
+ *    A failed launch returns PKV_ERR_CUDA.  Index errors only the device can
+ *    see (a table entry outside the pool, a slot past the pool, a context
+ *    longer than its table row) skip the offending work and set bits in a
+ *    device error word that pkv_get_device_error() reads back; kernels never
+ *    trap, assert or wait without a limit.
+ *  - Element types: PKV_F32, PKV_F16, PKV_BF16.  q, k_new and v_new have the
+ *    pool's element type.  Decode output is fp32 or the pool's type.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_INVALID = 1,      /* null pointer, bad size, misaligned pointer, Hq % Hkv != 0 ... */
+    PKV_ERR_UNSUPPORTED = 2,  /* valid but not built: head_dim, block size, group size, dtype */
+    PKV_ERR_WORKSPACE = 3,    /* partitioned decode without a large enough workspace */
+    PKV_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+    PKV_ERR_DEVICE = 5        /* pkv_get_device_error found error bits set */
+} pkv_status;
+
+typedef enum pkv_dtype { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2 } pkv_dtype;
+
+/* Bits of the device error word. */
+#define PKV_DEVERR_BLOCK_ID 0x1u  /* a block-table entry that a position needs is outside [0, num_blocks) */
+#define PKV_DEVERR_SLOT     0x2u  /* a slot at or past num_blocks * block_size */
+#define PKV_DEVERR_CONTEXT  0x4u  /* context_len < 0, > max_blocks_per_seq * B or > max_context_len */
+#define PKV_DEVERR_TIMEOUT  0x8u  /* a copy pipeline wait ran out of time (about 2 s) */
+#define PKV_DEVERR_POSITION 0x10u /* slot mapping: position past the table row, or bad sequence index */
+#define PKV_DEVERR_PAIR     0x20u /* copy_blocks: a src or dst outside [0, num_blocks) */
+
+/*
+ * The physical block pool: two caller-owned device arrays, K and V, each laid
+ * out [num_blocks][num_kv_heads][block_size][head_dim], row-major, head_dim
+ * innermost.  One (block, kv head) page is block_size * head_dim contiguous
+ * elements; one physical block across all kv heads is
+ * num_kv_heads * block_size * head_dim contiguous elements.  k and v must be
+ * 16-byte aligned.  Built: block_size in {16, 32}, head_dim in {64, 128}.
+ */
+typedef struct pkv_pool {
+    void* k;
+    void* v;
+    int32_t num_blocks;
+    int32_t block_size;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t dtype; /* pkv_dtype */
+} pkv_pool;
+
+/*
+ * Slot of each token to append: slot_mapping[t] = block_tables[s][p / B] * B + p % B,
+ * with s = token_seq[t] (or t when token_seq is NULL) and p = positions[t].
+ * "What Is vLLM", section "How does PagedAttention work?": the engine looks up
+ * which physical block holds a position and indexes into it.
+ *   block_tables  int32 [num_seqs][max_blocks_per_seq]
+ *   positions     int32 [num_tokens]; p < 0 gives slot -1 (padding)
+ *   token_seq     int32 [num_tokens] or NULL
+ *   slot_mapping  int64 [num_tokens] (output)
+ * Device errors: p / B >= max_blocks_per_seq or s outside [0, num_seqs)
+ * (PKV_DEVERR_POSITION), a negative table entry (PKV_DEVERR_BLOCK_ID); the
+ * slot is then -1.
+ */
+pkv_status pkv_slot_mapping(const int32_t* block_tables, int32_t max_blocks_per_seq,
+                            int32_t num_seqs, const int32_t* positions, const int32_t* token_seq,
+                            int32_t num_tokens, int32_t block_size, int64_t* slot_mapping,
+                            void* stream);
+
+/*
+ * Append new tokens: for each t with slot_mapping[t] >= 0 and every kv head h,
+ * k_pool[slot / B][h][slot % B][:] = k_new[t][h][:] and the same for V (bit
+ * copy).  "vLLM in Production", section "PagedAttention - Virtual Memory for
+ * the KV Cache": a sequence grows one block at a time as tokens arrive.
+ *   k_new, v_new   [num_tokens][num_kv_heads][head_dim] in the pool type, 16-byte aligned
+ *   slot_mapping   int64 [num_tokens]; negative = skip
+ * Slots within one call must be distinct.  A slot >= num_blocks * B is
+ * skipped and sets PKV_DEVERR_SLOT.
+ */
+pkv_status pkv_kv_cache_write(const pkv_pool* pool, const void* k_new, const void* v_new,
+                              const int64_t* slot_mapping, int32_t num_tokens, void* stream);
+
+/*
+ * Partition size (tokens) that pkv_paged_attention_decode uses when it is
+ * given partition_size = 0: a multiple of the block size; a value >=
+ * max_context_len means one pass with no workspace.  Returns 0 on bad input.
+ */
+int32_t pkv_choose_partition_size(const pkv_pool* pool, int32_t num_seqs, int32_t num_q_heads,
+                                  int32_t max_context_len);
+
+/*
+ * Workspace bytes a decode or partition call needs for these sizes
+ * (partition_size 0 = the automatic choice).  0 when one pass suffices.
+ * Layout, with P parts = ceil(max_context_len / partition_size) and
+ * R = num_seqs * num_q_heads rows, all fp32:
+ *   m [R][P]    at byte 0                    largest scaled score of the range
+ *   l [R][P]    at byte A = align16(4 R P)   sum of exp(score - m)
+ *   o [R][P][D] at byte 2 A                  sum of exp(score - m) * V, not divided by l
+ */
+size_t pkv_decode_workspace_bytes(const pkv_pool* pool, int32_t num_seqs, int32_t num_q_heads,
+                                  int32_t max_context_len, int32_t partition_size);
+
+/*
+ * Workspace bytes pkv_paged_attention_partitions needs: the layout above with
+ * ceil(max_context_len / partition_size) parts (at least one).  0 on bad input.
+ */
+size_t pkv_partition_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                     int32_t max_context_len, int32_t partition_size);
+
+/*
+ * Paged attention decode, one query row per sequence and q head:
+ *   out[s][h] = softmax(scale * q[s][h] . K_s^T) V_s
+ * over the context_lens[s] cached positions of sequence s, whose K and V rows
+ * are read in logical order through block_tables[s] from kv head
+ * h / (num_q_heads / num_kv_heads).  "vLLM in Production", section "The KV
+ * Cache and the 60-80% Memory Tax": each new token attends to every previous
+ * token through the cache.  context 0 gives a zero row.
+ *   q             [num_seqs][num_q_heads][head_dim], pool type, 16-byte aligned
+ *   block_tables  int32 [num_seqs][max_blocks_per_seq]; entries past
+ *                 ceil(context_lens[s] / B) are never read
+ *   context_lens  int32 [num_seqs]
+ *   max_context_len  host-side upper bound of context_lens (sizes the grid)
+ *   out           [num_seqs][num_q_heads][head_dim] of out_dtype (PKV_F32 or the pool type)
+ *   partition_size   0 = automatic; otherwise a multiple of block_size.  When
+ *                 ceil(max_context_len / partition_size) > 1 each partition of a
+ *                 sequence is reduced separately into the workspace and a
+ *                 log-sum-exp merge kernel writes out.
+ *   workspace     device memory of at least pkv_decode_workspace_bytes(...)
+ *                 bytes, 16-byte aligned, or NULL when none is needed.
+ * Built group sizes num_q_heads / num_kv_heads: 1, 2, 4, 8.
+ */
+pkv_status pkv_paged_attention_decode(const pkv_pool* pool, const void* q, int32_t num_seqs,
+                                      int32_t num_q_heads, const int32_t* block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                      int32_t max_context_len, float scale, void* out,
+                                      int32_t out_dtype, int32_t partition_size, void* workspace,
+                                      size_t workspace_bytes, void* stream);
+
+/*
+ * The partition step alone: for every sequence s, q head h and partition
+ * k < ceil(context_lens[s] / partition_size), writes (m, l, o) of tokens
+ * [k P, min(ctx, (k+1) P)) to the workspace in the layout above (a context
+ * of 0 writes m = -inf, l = 0, o = 0 at k = 0).  Lets a caller reduce token
+ * ranges separately (for example on several devices) and combine them with
+ * pkv_lse_merge.  partition_size > 0, a multiple of block_size.
+ */
+pkv_status pkv_paged_attention_partitions(const pkv_pool* pool, const void* q, int32_t num_seqs,
+                                          int32_t num_q_heads, const int32_t* block_tables,
+                                          int32_t max_blocks_per_seq,
+                                          const int32_t* context_lens, int32_t max_context_len,
+                                          float scale, int32_t partition_size, void* workspace,
+                                          size_t workspace_bytes, void* stream);
+
+/*
+ * Log-sum-exp merge of partition results (layout above):
+ *   M = max_k m_k,  out = sum_k exp(m_k - M) o_k / sum_k exp(m_k - M) l_k
+ * over k < ceil(context_lens[s] / partition_size); rows with no tokens give 0.
+ */
+pkv_status pkv_lse_merge(const void* workspace, size_t workspace_bytes, int32_t num_seqs,
+                         int32_t num_q_heads, int32_t head_dim, const int32_t* context_lens,
+                         int32_t max_context_len, int32_t partition_size, void* out,
+                         int32_t out_dtype, void* stream);
+
+/*
+ * Copy-on-write of shared blocks: for each pair i, physical block
+ * src_dst_pairs[2i+1] of both pools becomes a bit copy of block
+ * src_dst_pairs[2i] (all kv heads, all rows).  "What Is vLLM", section "How
+ * does PagedAttention work?", step "Memory sharing": blocks shared by several
+ * sequences are reference counted and copied on write.
+ *   src_dst_pairs  int32 [num_pairs][2] on the device
+ * dst blocks must be distinct and must not be sources in the same call.  A
+ * pair with an id outside the pool is skipped and sets PKV_DEVERR_PAIR.
+ */
+pkv_status pkv_copy_blocks(const pkv_pool* pool, const int32_t* src_dst_pairs, int32_t num_pairs,
+                           void* stream);
+
+/*
+ * Synchronises stream, then reads and clears the current device's error word
+ * into *flags (host pointer).  Returns PKV_ERR_DEVICE when any bit was set.
+ */
+pkv_status pkv_get_device_error(uint32_t* flags, void* stream);
+
+/* Static text for a status code. */
+const char* pkv_status_str(pkv_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

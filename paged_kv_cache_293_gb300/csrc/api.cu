@@ -1,0 +1,346 @@
+// api.cu -- the C ABI of libpagedkv.so (declared in include/pagedkv.h).
+//
+// Host-side argument checks, the choice of partition size, workspace layout,
+// dispatch to the typed kernels, and the device error word.  Nothing here
+// allocates device memory or synchronises, except pkv_get_device_error.
+#include <cmath>
+#include <cstdint>
+
+#include "pkv_common.cuh"
+
+namespace {
+
+// One word per device: kernels OR error bits into it instead of trapping.
+__device__ unsigned int g_error_word;
+
+constexpr int MAX_DEVICES = 64;
+unsigned int* g_error_ptr[MAX_DEVICES] = {nullptr};
+
+pkv_status error_word(unsigned int** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return PKV_ERR_CUDA;
+    if (!g_error_ptr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_error_word) != cudaSuccess) return PKV_ERR_CUDA;
+        g_error_ptr[dev] = static_cast<unsigned int*>(ptr);
+    }
+    *out = g_error_ptr[dev];
+    return PKV_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+pkv_status check_pool(const pkv_pool* pool) {
+    if (!pool || !pool->k || !pool->v) return PKV_ERR_INVALID;
+    if (!aligned16(pool->k) || !aligned16(pool->v)) return PKV_ERR_INVALID;
+    if (pool->num_blocks <= 0 || pool->block_size <= 0 || pool->num_kv_heads <= 0 ||
+        pool->head_dim <= 0)
+        return PKV_ERR_INVALID;
+    if (pool->dtype != PKV_F32 && pool->dtype != PKV_F16 && pool->dtype != PKV_BF16)
+        return PKV_ERR_INVALID;
+    if (pool->block_size != 16 && pool->block_size != 32) return PKV_ERR_UNSUPPORTED;
+    if (pool->head_dim != 64 && pool->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    return PKV_OK;
+}
+
+int32_t ceil_div(int64_t a, int64_t b) { return int32_t((a + b - 1) / b); }
+
+struct WsLayout {
+    size_t l_off, o_off, bytes;
+};
+
+WsLayout ws_layout(int32_t S, int32_t Hq, int32_t D, int32_t parts) {
+    const size_t rows = (size_t)S * Hq * parts;
+    const size_t a = (rows * 4 + 15) & ~size_t(15);
+    return WsLayout{a, 2 * a, 2 * a + rows * D * 4};
+}
+
+int32_t auto_partition(const pkv_pool* pool, int32_t max_context_len) {
+    const int32_t B = pool->block_size;
+    const int32_t split = 512;  // tokens per partition for long contexts (a multiple of 16 and 32)
+    if (max_context_len <= split) return max_context_len <= 0 ? B : ceil_div(max_context_len, B) * B;
+    return split;
+}
+
+struct DecodeArgs {
+    const pkv_pool* pool;
+    const void* q;
+    int32_t S, Hq;
+    const int32_t* bt;
+    int32_t M;
+    const int32_t* ctx;
+    int32_t max_ctx;
+    float scale;
+    int32_t P;  // 0 = auto
+};
+
+pkv_status check_decode(const DecodeArgs& a) {
+    pkv_status st = check_pool(a.pool);
+    if (st != PKV_OK) return st;
+    if (a.S < 0 || a.Hq <= 0 || a.M <= 0 || a.max_ctx < 0) return PKV_ERR_INVALID;
+    if (a.Hq % a.pool->num_kv_heads != 0) return PKV_ERR_INVALID;
+    if (!std::isfinite(a.scale)) return PKV_ERR_INVALID;
+    if (a.P < 0 || (a.P > 0 && a.P % a.pool->block_size != 0)) return PKV_ERR_INVALID;
+    if (a.S > 0 && (!a.q || !a.bt || !a.ctx)) return PKV_ERR_INVALID;
+    if (a.S > 0 && !aligned16(a.q)) return PKV_ERR_INVALID;
+    const int32_t G = a.Hq / a.pool->num_kv_heads;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return PKV_ERR_UNSUPPORTED;
+    if (a.S > 65535) return PKV_ERR_UNSUPPORTED;
+    return PKV_OK;
+}
+
+cudaError_t launch_decode_typed(const pkv::DecodeParams& p, int32_t dtype, int D, int G,
+                                cudaStream_t stream) {
+    switch (dtype) {
+        case PKV_F32: return pkv::launch_decode<float>(p, D, G, stream);
+        case PKV_F16: return pkv::launch_decode<__half>(p, D, G, stream);
+        default: return pkv::launch_decode<__nv_bfloat16>(p, D, G, stream);
+    }
+}
+
+// Shared body of decode (direct = 1) and the partition step (direct = 0).
+pkv_status run_decode(const DecodeArgs& a, void* out, int32_t out_dtype, int direct,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    const pkv_pool* pool = a.pool;
+    const int32_t P = a.P > 0 ? a.P : auto_partition(pool, a.max_ctx);
+    const int32_t parts = a.max_ctx > 0 ? ceil_div(a.max_ctx, P) : 1;
+    if (parts > 65535) return PKV_ERR_UNSUPPORTED;
+    const bool need_ws = !direct || parts > 1;
+    const WsLayout lay = ws_layout(a.S, a.Hq, pool->head_dim, parts);
+    if (need_ws && (!workspace || !aligned16(workspace) || workspace_bytes < lay.bytes))
+        return PKV_ERR_WORKSPACE;
+    if (a.S == 0) return PKV_OK;
+    unsigned int* err = nullptr;
+    pkv_status st = error_word(&err);
+    if (st != PKV_OK) return st;
+
+    pkv::DecodeParams p{};
+    p.k_pool = pool->k;
+    p.v_pool = pool->v;
+    p.num_blocks = pool->num_blocks;
+    p.block_size = pool->block_size;
+    p.num_kv_heads = pool->num_kv_heads;
+    p.q = a.q;
+    p.num_seqs = a.S;
+    p.num_q_heads = a.Hq;
+    p.block_tables = a.bt;
+    p.max_blocks_per_seq = a.M;
+    p.context_lens = a.ctx;
+    p.max_context_len = a.max_ctx;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.partition_size = P;
+    p.max_parts = parts;
+    p.out = out;
+    p.out_dtype = out_dtype;
+    p.direct_single = direct;
+    if (need_ws) {
+        char* ws = static_cast<char*>(workspace);
+        p.ws_m = reinterpret_cast<float*>(ws);
+        p.ws_l = reinterpret_cast<float*>(ws + lay.l_off);
+        p.ws_o = reinterpret_cast<float*>(ws + lay.o_off);
+    }
+    p.err = err;
+    const int G = a.Hq / pool->num_kv_heads;
+    if (launch_decode_typed(p, pool->dtype, pool->head_dim, G, stream) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    if (direct && parts > 1) {
+        pkv::MergeParams mp{};
+        mp.ws_m = p.ws_m;
+        mp.ws_l = p.ws_l;
+        mp.ws_o = p.ws_o;
+        mp.context_lens = a.ctx;
+        mp.num_seqs = a.S;
+        mp.num_q_heads = a.Hq;
+        mp.head_dim = pool->head_dim;
+        mp.max_parts = parts;
+        mp.partition_size = P;
+        mp.skip_single = 1;
+        mp.out = out;
+        mp.out_dtype = out_dtype;
+        mp.err = err;
+        if (pkv::launch_merge(mp, stream) != cudaSuccess) return PKV_ERR_CUDA;
+    }
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t pkv_version(void) { return 100; }
+
+const char* pkv_status_str(pkv_status status) {
+    switch (status) {
+        case PKV_OK: return "ok";
+        case PKV_ERR_INVALID: return "invalid argument";
+        case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
+        case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+        case PKV_ERR_CUDA: return "CUDA error";
+        case PKV_ERR_DEVICE: return "device error flags set";
+    }
+    return "unknown status";
+}
+
+pkv_status pkv_slot_mapping(const int32_t* block_tables, int32_t max_blocks_per_seq,
+                            int32_t num_seqs, const int32_t* positions, const int32_t* token_seq,
+                            int32_t num_tokens, int32_t block_size, int64_t* slot_mapping,
+                            void* stream) {
+    if (num_tokens < 0 || block_size <= 0 || max_blocks_per_seq <= 0 || num_seqs < 0)
+        return PKV_ERR_INVALID;
+    if (num_tokens == 0) return PKV_OK;
+    if (!block_tables || !positions || !slot_mapping || num_seqs == 0) return PKV_ERR_INVALID;
+    if (!token_seq && num_tokens > num_seqs) return PKV_ERR_INVALID;
+    unsigned int* err = nullptr;
+    pkv_status st = error_word(&err);
+    if (st != PKV_OK) return st;
+    return pkv::launch_slot_mapping(block_tables, max_blocks_per_seq, num_seqs, positions,
+                                    token_seq, num_tokens, block_size, slot_mapping, err,
+                                    static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PKV_OK
+               : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_kv_cache_write(const pkv_pool* pool, const void* k_new, const void* v_new,
+                              const int64_t* slot_mapping, int32_t num_tokens, void* stream) {
+    pkv_status st = check_pool(pool);
+    if (st != PKV_OK) return st;
+    if (num_tokens < 0) return PKV_ERR_INVALID;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k_new || !v_new || !slot_mapping || !aligned16(k_new) || !aligned16(v_new))
+        return PKV_ERR_INVALID;
+    unsigned int* err = nullptr;
+    st = error_word(&err);
+    if (st != PKV_OK) return st;
+    return pkv::launch_cache_write(*pool, k_new, v_new, slot_mapping, num_tokens, err,
+                                   static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PKV_OK
+               : PKV_ERR_CUDA;
+}
+
+int32_t pkv_choose_partition_size(const pkv_pool* pool, int32_t num_seqs, int32_t num_q_heads,
+                                  int32_t max_context_len) {
+    (void)num_seqs;
+    (void)num_q_heads;
+    if (!pool || pool->block_size <= 0 || max_context_len < 0) return 0;
+    return auto_partition(pool, max_context_len);
+}
+
+size_t pkv_decode_workspace_bytes(const pkv_pool* pool, int32_t num_seqs, int32_t num_q_heads,
+                                  int32_t max_context_len, int32_t partition_size) {
+    if (!pool || pool->block_size <= 0 || pool->head_dim <= 0 || num_seqs < 0 ||
+        num_q_heads <= 0 || max_context_len < 0 || partition_size < 0)
+        return 0;
+    const int32_t P = partition_size > 0 ? partition_size : auto_partition(pool, max_context_len);
+    const int32_t parts = max_context_len > 0 ? ceil_div(max_context_len, P) : 1;
+    if (parts <= 1) return 0;
+    return ws_layout(num_seqs, num_q_heads, pool->head_dim, parts).bytes;
+}
+
+size_t pkv_partition_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                     int32_t max_context_len, int32_t partition_size) {
+    if (num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0 || max_context_len < 0 ||
+        partition_size <= 0)
+        return 0;
+    const int32_t parts = max_context_len > 0 ? ceil_div(max_context_len, partition_size) : 1;
+    return ws_layout(num_seqs, num_q_heads, head_dim, parts).bytes;
+}
+
+pkv_status pkv_paged_attention_decode(const pkv_pool* pool, const void* q, int32_t num_seqs,
+                                      int32_t num_q_heads, const int32_t* block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                      int32_t max_context_len, float scale, void* out,
+                                      int32_t out_dtype, int32_t partition_size, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+    DecodeArgs a{pool, q, num_seqs, num_q_heads, block_tables, max_blocks_per_seq,
+                 context_lens, max_context_len, scale, partition_size};
+    pkv_status st = check_decode(a);
+    if (st != PKV_OK) return st;
+    if (num_seqs > 0 && !out) return PKV_ERR_INVALID;
+    if (out_dtype != PKV_F32 && out_dtype != pool->dtype) return PKV_ERR_UNSUPPORTED;
+    return run_decode(a, out, out_dtype, 1, workspace, workspace_bytes,
+                      static_cast<cudaStream_t>(stream));
+}
+
+pkv_status pkv_paged_attention_partitions(const pkv_pool* pool, const void* q, int32_t num_seqs,
+                                          int32_t num_q_heads, const int32_t* block_tables,
+                                          int32_t max_blocks_per_seq,
+                                          const int32_t* context_lens, int32_t max_context_len,
+                                          float scale, int32_t partition_size, void* workspace,
+                                          size_t workspace_bytes, void* stream) {
+    DecodeArgs a{pool, q, num_seqs, num_q_heads, block_tables, max_blocks_per_seq,
+                 context_lens, max_context_len, scale, partition_size};
+    pkv_status st = check_decode(a);
+    if (st != PKV_OK) return st;
+    if (partition_size <= 0) return PKV_ERR_INVALID;
+    return run_decode(a, nullptr, PKV_F32, 0, workspace, workspace_bytes,
+                      static_cast<cudaStream_t>(stream));
+}
+
+pkv_status pkv_lse_merge(const void* workspace, size_t workspace_bytes, int32_t num_seqs,
+                         int32_t num_q_heads, int32_t head_dim, const int32_t* context_lens,
+                         int32_t max_context_len, int32_t partition_size, void* out,
+                         int32_t out_dtype, void* stream) {
+    if (num_seqs < 0 || num_q_heads <= 0 || max_context_len < 0 || partition_size <= 0)
+        return PKV_ERR_INVALID;
+    if (out_dtype != PKV_F32 && out_dtype != PKV_F16 && out_dtype != PKV_BF16)
+        return PKV_ERR_INVALID;
+    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PKV_OK;
+    if (!context_lens || !out) return PKV_ERR_INVALID;
+    const int32_t parts = max_context_len > 0 ? ceil_div(max_context_len, partition_size) : 1;
+    const WsLayout lay = ws_layout(num_seqs, num_q_heads, head_dim, parts);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < lay.bytes) return PKV_ERR_WORKSPACE;
+    unsigned int* err = nullptr;
+    pkv_status st = error_word(&err);
+    if (st != PKV_OK) return st;
+    const char* ws = static_cast<const char*>(workspace);
+    pkv::MergeParams mp{};
+    mp.ws_m = reinterpret_cast<const float*>(ws);
+    mp.ws_l = reinterpret_cast<const float*>(ws + lay.l_off);
+    mp.ws_o = reinterpret_cast<const float*>(ws + lay.o_off);
+    mp.context_lens = context_lens;
+    mp.num_seqs = num_seqs;
+    mp.num_q_heads = num_q_heads;
+    mp.head_dim = head_dim;
+    mp.max_parts = parts;
+    mp.partition_size = partition_size;
+    mp.skip_single = 0;
+    mp.out = out;
+    mp.out_dtype = out_dtype;
+    mp.err = err;
+    return pkv::launch_merge(mp, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK
+                                                                                 : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_copy_blocks(const pkv_pool* pool, const int32_t* src_dst_pairs, int32_t num_pairs,
+                           void* stream) {
+    pkv_status st = check_pool(pool);
+    if (st != PKV_OK) return st;
+    if (num_pairs < 0) return PKV_ERR_INVALID;
+    if (num_pairs == 0) return PKV_OK;
+    if (!src_dst_pairs) return PKV_ERR_INVALID;
+    unsigned int* err = nullptr;
+    st = error_word(&err);
+    if (st != PKV_OK) return st;
+    return pkv::launch_copy_blocks(*pool, src_dst_pairs, num_pairs, err,
+                                   static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PKV_OK
+               : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_get_device_error(uint32_t* flags, void* stream) {
+    if (!flags) return PKV_ERR_INVALID;
+    unsigned int* err = nullptr;
+    pkv_status st = error_word(&err);
+    if (st != PKV_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int host = 0;
+    if (cudaMemcpyAsync(&host, err, sizeof(host), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemsetAsync(err, 0, sizeof(unsigned int), s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    *flags = host;
+    return host ? PKV_ERR_DEVICE : PKV_OK;
+}
+
+}  // extern "C"

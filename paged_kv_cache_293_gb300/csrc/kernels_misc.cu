@@ -1,0 +1,197 @@
+// kernels_misc.cu -- slot mapping, cache write, copy-on-write block copy and the
+// log-sum-exp merge of partitioned decode.
+#include <cmath>
+
+#include "pkv_common.cuh"
+
+namespace pkv {
+
+// ------------------------------------------------------------------ slot mapping
+// "What Is vLLM", section "How does PagedAttention work?": the physical block
+// that holds position p is the table entry of logical block p / B; the row is p % B.
+__global__ void slot_mapping_kernel(const int32_t* __restrict__ block_tables, int32_t M,
+                                    int32_t S, const int32_t* __restrict__ positions,
+                                    const int32_t* __restrict__ token_seq, int32_t T, int32_t B,
+                                    int64_t* __restrict__ slots, unsigned int* err) {
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= T) return;
+    const int s = token_seq ? token_seq[t] : t;
+    const int p = positions[t];
+    if (p < 0) { slots[t] = -1; return; }
+    const int j = p / B;
+    if (s < 0 || s >= S || j >= M) {
+        set_error(err, PKV_DEVERR_POSITION);
+        slots[t] = -1;
+        return;
+    }
+    const int phys = block_tables[(size_t)s * M + j];
+    if (phys < 0) {
+        set_error(err, PKV_DEVERR_BLOCK_ID);
+        slots[t] = -1;
+        return;
+    }
+    slots[t] = (int64_t)phys * B + (p - j * B);
+}
+
+cudaError_t launch_slot_mapping(const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                int32_t num_seqs, const int32_t* positions,
+                                const int32_t* token_seq, int32_t num_tokens, int32_t block_size,
+                                int64_t* slot_mapping, unsigned int* err, cudaStream_t stream) {
+    const int threads = 128;
+    const int blocks = (num_tokens + threads - 1) / threads;
+    slot_mapping_kernel<<<blocks, threads, 0, stream>>>(block_tables, max_blocks_per_seq, num_seqs,
+                                                        positions, token_seq, num_tokens,
+                                                        block_size, slot_mapping, err);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ cache write
+// One thread per 16-byte vector of a (token, kv head) row, for K and V.
+__global__ void cache_write_kernel(uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
+                                   const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+                                   const int64_t* __restrict__ slots, int32_t T, int32_t Hkv,
+                                   int32_t B, int32_t vpr, long long num_slots,
+                                   unsigned int* err) {
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long per_tok = (long long)Hkv * vpr;
+    if (idx >= (long long)T * per_tok) return;
+    const int t = int(idx / per_tok);
+    const int rem = int(idx - (long long)t * per_tok);
+    const int h = rem / vpr, v = rem - h * vpr;
+    const long long slot = slots[t];
+    if (slot < 0) return;
+    if (slot >= num_slots) {
+        if (rem == 0) set_error(err, PKV_DEVERR_SLOT);
+        return;
+    }
+    const long long blk = slot / B, row = slot - blk * B;
+    const size_t dst = (size_t)(((blk * Hkv + h) * B + row) * vpr + v);
+    const uint4 kv = k_new[idx];
+    const uint4 vv = v_new[idx];
+    k_pool[dst] = kv;
+    v_pool[dst] = vv;
+}
+
+static int elem_bytes(int32_t dtype) { return dtype == PKV_F32 ? 4 : 2; }
+
+cudaError_t launch_cache_write(const pkv_pool& pool, const void* k_new, const void* v_new,
+                               const int64_t* slot_mapping, int32_t num_tokens, unsigned int* err,
+                               cudaStream_t stream) {
+    const int vpr = pool.head_dim * elem_bytes(pool.dtype) / 16;
+    const long long total = (long long)num_tokens * pool.num_kv_heads * vpr;
+    const int threads = 256;
+    const long long blocks = (total + threads - 1) / threads;
+    cache_write_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
+        static_cast<uint4*>(pool.k), static_cast<uint4*>(pool.v),
+        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping,
+        num_tokens, pool.num_kv_heads, pool.block_size, vpr,
+        (long long)pool.num_blocks * pool.block_size, err);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ copy-on-write block copy
+// "What Is vLLM", section "How does PagedAttention work?", step "Memory sharing".
+// grid = (pairs, slices of a block, 2 pools); 16-byte vectors.
+__global__ void copy_blocks_kernel(uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
+                                   int32_t num_blocks, long long vec_per_block,
+                                   const int32_t* __restrict__ pairs, unsigned int* err) {
+    const int i = blockIdx.x;
+    const int src = pairs[2 * i], dst = pairs[2 * i + 1];
+    if ((unsigned)src >= (unsigned)num_blocks || (unsigned)dst >= (unsigned)num_blocks) {
+        if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) set_error(err, PKV_DEVERR_PAIR);
+        return;
+    }
+    uint4* pool = blockIdx.z == 0 ? k_pool : v_pool;
+    const uint4* from = pool + (size_t)src * vec_per_block;
+    uint4* to = pool + (size_t)dst * vec_per_block;
+    for (long long j = (long long)blockIdx.y * blockDim.x + threadIdx.x; j < vec_per_block;
+         j += (long long)gridDim.y * blockDim.x)
+        to[j] = from[j];
+}
+
+cudaError_t launch_copy_blocks(const pkv_pool& pool, const int32_t* pairs, int32_t num_pairs,
+                               unsigned int* err, cudaStream_t stream) {
+    const long long vec = (long long)pool.num_kv_heads * pool.block_size * pool.head_dim *
+                          elem_bytes(pool.dtype) / 16;
+    const int threads = 256;
+    long long slices = (vec + threads * 4 - 1) / (threads * 4);
+    if (slices > 65535) slices = 65535;
+    dim3 grid((unsigned)num_pairs, (unsigned)slices, 2);
+    copy_blocks_kernel<<<grid, threads, 0, stream>>>(static_cast<uint4*>(pool.k),
+                                                     static_cast<uint4*>(pool.v), pool.num_blocks,
+                                                     vec, pairs, err);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ log-sum-exp merge
+// Row (s, h) with n = ceil(ctx / P) partitions:  M = max_k m_k,
+// out = sum_k e^(m_k - M) o_k / sum_k e^(m_k - M) l_k.  One CTA (4 warps) per row;
+// warp w takes partitions k = w, w + 4, ...; lane j holds dims j, j + 32, ...
+template <int D>
+__global__ void __launch_bounds__(128) lse_merge_kernel(const MergeParams p) {
+    constexpr int NWM = 4, DPL = D / 32;
+    __shared__ float red[NWM][D + 1];
+    __shared__ float smax[NWM];
+    const int row = blockIdx.x;
+    const int s = row / p.num_q_heads;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int ctx = p.context_lens[s];
+    const long long cap = (long long)p.max_parts * p.partition_size;
+    if (ctx < 0) ctx = 0;
+    if (ctx > cap) ctx = int(cap);
+    const int n = (ctx + p.partition_size - 1) / p.partition_size;
+    if (p.skip_single && n <= 1) return;
+    const float* mrow = p.ws_m + (size_t)row * p.max_parts;
+    const float* lrow = p.ws_l + (size_t)row * p.max_parts;
+    const float* orow = p.ws_o + (size_t)row * p.max_parts * D;
+
+    float M = -INFINITY;
+    for (int k = threadIdx.x; k < n; k += NWM * 32)
+        if (lrow[k] > 0.f) M = fmaxf(M, mrow[k]);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL_MASK, M, o));
+    if (lane == 0) smax[warp] = M;
+    __syncthreads();
+    M = fmaxf(fmaxf(smax[0], smax[1]), fmaxf(smax[2], smax[3]));
+    const size_t out_base = (size_t)row * D;
+    if (M == -INFINITY) {
+        for (int d = threadIdx.x; d < D; d += NWM * 32) store_out(p.out, p.out_dtype, out_base + d, 0.f);
+        return;
+    }
+    const float log2e = 1.4426950408889634f;
+    float L = 0.f, O[DPL];
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) O[j] = 0.f;
+#pragma unroll 4
+    for (int k = warp; k < n; k += NWM) {
+        const float lk = lrow[k];
+        const float w = lk > 0.f ? fast_exp2((mrow[k] - M) * log2e) : 0.f;
+        L = fmaf(w, lk, L);
+#pragma unroll
+        for (int j = 0; j < DPL; ++j) O[j] = fmaf(w, orow[(size_t)k * D + lane + 32 * j], O[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) red[warp][lane + 32 * j] = O[j];
+    if (lane == 0) red[warp][D] = L;
+    __syncthreads();
+    for (int d = threadIdx.x; d < D; d += NWM * 32) {
+        float num = 0.f, den = 0.f;
+#pragma unroll
+        for (int w = 0; w < NWM; ++w) { num += red[w][d]; den += red[w][D]; }
+        store_out(p.out, p.out_dtype, out_base + d, num / den);
+    }
+}
+
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
+    const unsigned rows = (unsigned)((long long)p.num_seqs * p.num_q_heads);
+    if (rows == 0) return cudaSuccess;
+    if (p.head_dim == 64)
+        lse_merge_kernel<64><<<rows, 128, 0, stream>>>(p);
+    else if (p.head_dim == 128)
+        lse_merge_kernel<128><<<rows, 128, 0, stream>>>(p);
+    else
+        return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

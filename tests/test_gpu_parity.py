@@ -1,0 +1,305 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 CPU oracle.
+
+Bit-exact for slot mapping, cache write and block copy; max-abs 1e-5 (fp32
+KV) / 2e-3 (fp16, bf16 KV) for attention with fp32 output; a 16-bit output
+must equal the oracle rounded to that type within one unit in the last place.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_293_gb300 import workloads
+from gpu_helpers import TOL, compact_for_oracle, dev_i32, host, max_abs, pkv
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def P():
+    return pkv()
+
+
+def run_decode(P, w, partition_size=None, out_dtype=torch.float32, block_tables=None,
+               context_lens=None, max_context_len=None):
+    bt = dev_i32(w.block_tables if block_tables is None else block_tables)
+    ctx_np = w.context_lens if context_lens is None else context_lens
+    ctx = dev_i32(ctx_np)
+    mcl = int(np.max(ctx_np, initial=0)) if max_context_len is None else max_context_len
+    ps = w.partition_size if partition_size is None else partition_size
+    out = torch.full((w.num_seqs, w.num_q_heads, w.head_dim), float("nan"), dtype=out_dtype,
+                     device=DEV)
+    ws_bytes = P.pkv_decode_workspace_bytes(w.k_pool, w.num_seqs, w.num_q_heads, mcl, ps)
+    ws = P.workspace_tensor(ws_bytes, DEV) if ws_bytes else None
+    P.pkv_paged_attention_decode(w.q, w.k_pool, w.v_pool, bt, ctx, w.scale, out, mcl, ps, ws)
+    torch.cuda.synchronize()
+    return out
+
+
+def oracle_decode(w, block_tables=None):
+    bt = w.block_tables if block_tables is None else block_tables
+    return oracle.paged_decode(w.dtype, host(w.k_pool), host(w.v_pool), host(w.q), bt,
+                               w.context_lens, w.scale)
+
+
+def assert_no_device_error(P):
+    assert P.pkv_get_device_error() == 0
+
+
+# ------------------------------------------------------------------ small, many shapes
+
+SMALL = [
+    # dtype, Hq, Hkv, D, B, context lengths (ragged, partial chunks, 1 token, empty)
+    ("f32", 4, 4, 64, 16, [1, 17, 50, 100]),
+    ("f32", 8, 2, 128, 32, [0, 33, 64, 300, 15]),
+    ("f16", 8, 8, 128, 16, [1, 16, 17, 31, 32, 33, 511, 513, 1000]),
+    ("f16", 16, 2, 64, 32, [5, 64, 65, 700]),
+    ("bf16", 32, 8, 128, 16, [3, 48, 160, 1100]),
+    ("bf16", 8, 1, 64, 16, [2, 250]),
+    ("f16", 32, 4, 128, 32, [90, 1999]),
+]
+
+
+@pytest.mark.parametrize("dtype,Hq,Hkv,D,B,ctx", SMALL)
+@pytest.mark.parametrize("psize", [0, 64, 512, 4096])
+def test_decode_matches_oracle_small(P, dtype, Hq, Hkv, D, B, ctx, psize):
+    if psize and psize % B:
+        pytest.skip("partition must be a multiple of the block size")
+    w = workloads.build("small", dtype=dtype, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                        block_size=B, context_lens=ctx, seed=len(ctx) + D, device=DEV)
+    got = run_decode(P, w, partition_size=psize)
+    ref = oracle_decode(w)
+    assert max_abs(got, ref) <= TOL[dtype]
+    assert_no_device_error(P)
+
+
+def test_split_equals_single_pass(P):
+    w = workloads.build("split", dtype="f16", num_q_heads=16, num_kv_heads=4, head_dim=128,
+                        block_size=16, context_lens=[4000, 700, 1, 2048, 513], seed=3, device=DEV)
+    single = run_decode(P, w, partition_size=4096)
+    for ps in (16, 128, 512, 1024):
+        split = run_decode(P, w, partition_size=ps)
+        assert max_abs(split, single.double().cpu().numpy()) <= 1e-5
+    assert_no_device_error(P)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_16bit_output_is_oracle_rounded_within_one_ulp(P, dtype):
+    w = workloads.build("out16", dtype=dtype, num_q_heads=8, num_kv_heads=2, head_dim=128,
+                        block_size=16, context_lens=[7, 300, 1500], seed=5, device=DEV)
+    tdt = workloads.TORCH_DTYPE[dtype]
+    got = run_decode(P, w, out_dtype=tdt, partition_size=512).float().cpu()
+    ref = torch.from_numpy(oracle_decode(w))
+    ref_r = ref.to(tdt).float()
+    ulp = (ref_r.abs().clamp_min(1e-30).log2().floor().exp2()) * (2.0 ** -10 if dtype == "f16" else 2.0 ** -7)
+    assert torch.all((got - ref_r).abs() <= ulp + 1e-12)
+
+
+def test_block_permutation_gives_bit_identical_output(P):
+    w = workloads.build("perm", dtype="bf16", num_q_heads=32, num_kv_heads=8, head_dim=128,
+                        block_size=16, context_lens=[40, 900, 1234, 17], seed=8, device=DEV)
+    base = run_decode(P, w, partition_size=512)
+    perm = torch.randperm(w.num_blocks, generator=torch.Generator().manual_seed(1))
+    k2 = torch.empty_like(w.k_pool)
+    v2 = torch.empty_like(w.v_pool)
+    k2[perm.to(DEV)] = w.k_pool
+    v2[perm.to(DEV)] = w.v_pool
+    bt = np.where(w.block_tables >= 0, perm.numpy()[np.maximum(w.block_tables, 0)], -1)
+    w.k_pool, w.v_pool = k2, v2
+    moved = run_decode(P, w, partition_size=512, block_tables=bt)
+    assert torch.equal(base, moved)
+
+
+def test_partitions_and_merge_match_oracle(P):
+    w = workloads.build("parts", dtype="f16", num_q_heads=8, num_kv_heads=4, head_dim=64,
+                        block_size=16, context_lens=[0, 5, 512, 1025, 2000], seed=9, device=DEV)
+    Pz, mcl = 256, int(w.context_lens.max())
+    nparts = -(-mcl // Pz)
+    ws = P.workspace_tensor(P.pkv_partition_workspace_bytes(w.num_seqs, w.num_q_heads,
+                                                            w.head_dim, mcl, Pz), DEV)
+    ctx = dev_i32(w.context_lens)
+    P.pkv_paged_attention_partitions(w.q, w.k_pool, w.v_pool, dev_i32(w.block_tables), ctx,
+                                     w.scale, mcl, Pz, ws)
+    torch.cuda.synchronize()
+    rows = w.num_seqs * w.num_q_heads * nparts
+    a = (rows * 4 + 15) // 16 * 16
+    wsf = ws.cpu().numpy()
+    m = wsf[:rows * 4].view(np.float32).reshape(w.num_seqs, w.num_q_heads, nparts)
+    l = wsf[a:a + rows * 4].view(np.float32).reshape(w.num_seqs, w.num_q_heads, nparts)
+    o = wsf[2 * a:2 * a + rows * w.head_dim * 4].view(np.float32).reshape(
+        w.num_seqs, w.num_q_heads, nparts, w.head_dim)
+    rm, rl, ro = oracle.partition_decode(w.dtype, host(w.k_pool), host(w.v_pool), host(w.q),
+                                         w.block_tables, w.context_lens, w.scale, Pz, nparts)
+    for s, c in enumerate(w.context_lens):
+        k = max(1, -(-int(c) // Pz))
+        if c == 0:
+            assert np.all(l[s, :, 0] == 0) and np.all(np.isneginf(m[s, :, 0]))
+            continue
+        np.testing.assert_allclose(m[s, :, :k], rm[s, :, :k], atol=2e-5, rtol=0)
+        np.testing.assert_allclose(l[s, :, :k], rl[s, :, :k], rtol=2e-5, atol=0)
+        np.testing.assert_allclose(o[s, :, :k] / l[s, :, :k, None],
+                                   ro[s, :, :k] / rl[s, :, :k, None], atol=2e-3, rtol=0)
+    # the merge entry point on the oracle's own partial results
+    ws2 = torch.zeros_like(ws)
+    buf = np.zeros(ws.numel(), np.uint8)
+    rm2 = np.where(np.isneginf(rm), -np.inf, rm).astype(np.float32)
+    buf[:rows * 4] = rm2.ravel().view(np.uint8)
+    buf[a:a + rows * 4] = rl.astype(np.float32).ravel().view(np.uint8)
+    buf[2 * a:2 * a + rows * w.head_dim * 4] = ro.astype(np.float32).ravel().view(np.uint8)
+    ws2.copy_(torch.from_numpy(buf))
+    out = torch.empty((w.num_seqs, w.num_q_heads, w.head_dim), dtype=torch.float32, device=DEV)
+    P.pkv_lse_merge(ws2, w.num_seqs, w.num_q_heads, w.head_dim, ctx, mcl, Pz, out)
+    torch.cuda.synchronize()
+    ref = oracle.lse_merge(rm, rl, ro)
+    assert max_abs(out, ref) <= 1e-5
+    assert_no_device_error(P)
+
+
+# ------------------------------------------------------------------ write, slot mapping, copy
+
+@pytest.mark.parametrize("dtype,B,D", [("f32", 16, 64), ("f16", 32, 128), ("bf16", 16, 128)])
+def test_slot_mapping_and_write_bit_exact(P, dtype, B, D):
+    w = workloads.build("write", dtype=dtype, num_q_heads=8, num_kv_heads=8, head_dim=D,
+                        block_size=B, context_lens=[1, 16, 17, 33, 200, 64], seed=2, device=DEV)
+    pos = w.positions.copy()
+    pos[3] = -1                                   # a padding token
+    slots = torch.empty(w.num_seqs, dtype=torch.int64, device=DEV)
+    P.pkv_slot_mapping(dev_i32(w.block_tables), dev_i32(pos), B, slots)
+    torch.cuda.synchronize()
+    ref_slots = oracle.slot_mapping(w.block_tables, pos, B)
+    assert np.array_equal(slots.cpu().numpy(), ref_slots)
+    k_ref, v_ref = host(w.k_pool).copy(), host(w.v_pool).copy()
+    oracle.kv_cache_write(dtype, k_ref, v_ref, host(w.k_new), host(w.v_new), ref_slots)
+    P.pkv_kv_cache_write(w.k_pool, w.v_pool, w.k_new, w.v_new, slots)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(w.k_pool), k_ref) and np.array_equal(host(w.v_pool), v_ref)
+    assert_no_device_error(P)
+
+
+def test_slot_mapping_with_token_sequence_index(P):
+    bt = np.array([[3, 1, -1], [0, 2, 4]], np.int32)
+    pos = np.array([0, 15, 16, 17, 40, -1], np.int32)
+    seq = np.array([0, 1, 0, 1, 1, 0], np.int32)
+    slots = torch.empty(6, dtype=torch.int64, device=DEV)
+    P.pkv_slot_mapping(dev_i32(bt), dev_i32(pos), 16, slots, token_seq=dev_i32(seq))
+    torch.cuda.synchronize()
+    assert np.array_equal(slots.cpu().numpy(), oracle.slot_mapping(bt, pos, 16, token_seq=seq))
+
+
+def test_copy_blocks_bit_exact_and_cow_is_a_no_op(P):
+    w = workloads.build("cow", dtype="bf16", num_q_heads=32, num_kv_heads=8, head_dim=128,
+                        block_size=16, context_lens=list(range(520, 1800, 80)), seed=4,
+                        device=DEV, shared_prefix_blocks=32, cow_fraction=0.25)
+    before = run_decode(P, w, partition_size=512)
+    k_ref, v_ref = host(w.k_pool).copy(), host(w.v_pool).copy()
+    oracle.copy_blocks(k_ref, v_ref, w.cow_pairs)
+    P.pkv_copy_blocks(w.k_pool, w.v_pool, dev_i32(w.cow_pairs))
+    torch.cuda.synchronize()
+    assert np.array_equal(host(w.k_pool), k_ref) and np.array_equal(host(w.v_pool), v_ref)
+    after = run_decode(P, w, partition_size=512, block_tables=w.block_tables_after_cow())
+    assert torch.equal(before, after)
+    assert_no_device_error(P)
+
+
+# ------------------------------------------------------------------ device-side error reporting
+
+def test_bad_block_id_sets_flag_without_faulting(P):
+    w = workloads.build("bad", dtype="f16", num_q_heads=4, num_kv_heads=4, head_dim=128,
+                        block_size=16, context_lens=[40, 40], seed=1, device=DEV)
+    bt = w.block_tables.copy()
+    bt[1, 1] = w.num_blocks + 5                    # outside the pool
+    run_decode(P, w, partition_size=0, block_tables=bt)
+    assert P.pkv_get_device_error() & P.DEVERR["BLOCK_ID"]
+    assert P.pkv_get_device_error() == 0           # reading clears it
+
+
+def test_slot_past_pool_sets_flag(P):
+    w = workloads.build("badslot", dtype="f16", num_q_heads=4, num_kv_heads=4, head_dim=128,
+                        block_size=16, context_lens=[5], seed=1, device=DEV)
+    k0 = w.k_pool.clone()
+    slots = torch.tensor([w.num_blocks * 16 + 3], dtype=torch.int64, device=DEV)
+    P.pkv_kv_cache_write(w.k_pool, w.v_pool, w.k_new, w.v_new, slots)
+    assert P.pkv_get_device_error() & P.DEVERR["SLOT"]
+    assert torch.equal(k0, w.k_pool)
+
+
+def test_context_beyond_table_sets_flag(P):
+    w = workloads.build("badctx", dtype="f16", num_q_heads=4, num_kv_heads=4, head_dim=128,
+                        block_size=16, context_lens=[30], seed=1, device=DEV)
+    run_decode(P, w, partition_size=0, context_lens=np.array([100], np.int32), max_context_len=100)
+    assert P.pkv_get_device_error() & P.DEVERR["CONTEXT"]
+
+
+def test_host_checks_return_status_before_launch(P):
+    w = workloads.build("args", dtype="f16", num_q_heads=6, num_kv_heads=4, head_dim=128,
+                        block_size=16, context_lens=[30], seed=1, device=DEV)
+    out = torch.empty((1, 6, 128), device=DEV)
+    with pytest.raises(P.PagedKVError) as e:   # 6 % 4 != 0
+        P.pkv_paged_attention_decode(w.q, w.k_pool, w.v_pool, dev_i32(w.block_tables),
+                                     dev_i32(w.context_lens), w.scale, out, 30)
+    assert e.value.status == P.PKV_ERR_INVALID
+    w2 = workloads.build("args2", dtype="f16", num_q_heads=8, num_kv_heads=4, head_dim=128,
+                         block_size=16, context_lens=[3000], seed=1, device=DEV)
+    out2 = torch.empty((1, 8, 128), device=DEV)
+    with pytest.raises(P.PagedKVError) as e:   # needs a workspace
+        P.pkv_paged_attention_decode(w2.q, w2.k_pool, w2.v_pool, dev_i32(w2.block_tables),
+                                     dev_i32(w2.context_lens), w2.scale, out2, 3000, 512, None)
+    assert e.value.status == P.PKV_ERR_WORKSPACE
+
+
+# ------------------------------------------------------------------ the five batches at full size
+
+def full_step(P, w):
+    """slot mapping -> cache write -> decode, as one decode step of a layer runs it."""
+    bt = dev_i32(w.block_tables)
+    pos = dev_i32(w.positions)
+    ctx = dev_i32(w.context_lens)
+    slots = torch.empty(w.num_seqs, dtype=torch.int64, device=DEV)
+    P.pkv_slot_mapping(bt, pos, w.block_size, slots)
+    P.pkv_kv_cache_write(w.k_pool, w.v_pool, w.k_new, w.v_new, slots)
+    out = torch.empty((w.num_seqs, w.num_q_heads, w.head_dim), dtype=torch.float32, device=DEV)
+    mcl = w.max_context_len
+    ws_bytes = P.pkv_decode_workspace_bytes(w.k_pool, w.num_seqs, w.num_q_heads, mcl,
+                                            w.partition_size)
+    ws = P.workspace_tensor(ws_bytes, DEV) if ws_bytes else None
+    P.pkv_paged_attention_decode(w.q, w.k_pool, w.v_pool, bt, ctx, w.scale, out, mcl,
+                                 w.partition_size, ws)
+    torch.cuda.synchronize()
+    return slots, out
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama7b", "llama13b_b16", "llama13b_b32", "gqa_prefix"])
+def test_full_config_step_matches_oracle(P, name):
+    w = workloads.make(name, seed=0, device=DEV)
+    k0, v0 = host(w.k_pool).copy(), host(w.v_pool).copy()
+    slots, out = full_step(P, w)
+    ref_slots = oracle.slot_mapping(w.block_tables, w.positions, w.block_size)
+    assert np.array_equal(slots.cpu().numpy(), ref_slots)
+    oracle.kv_cache_write(w.dtype, k0, v0, host(w.k_new), host(w.v_new), ref_slots)
+    assert np.array_equal(host(w.k_pool), k0) and np.array_equal(host(w.v_pool), v0)
+    ref = oracle.paged_decode(w.dtype, k0, v0, host(w.q), w.block_tables, w.context_lens, w.scale)
+    assert max_abs(out, ref) <= TOL[w.dtype]
+    if len(w.cow_pairs):
+        P.pkv_copy_blocks(w.k_pool, w.v_pool, dev_i32(w.cow_pairs))
+        oracle.copy_blocks(k0, v0, w.cow_pairs)
+        torch.cuda.synchronize()
+        assert np.array_equal(host(w.k_pool), k0) and np.array_equal(host(w.v_pool), v0)
+        after = run_decode(P, w, block_tables=w.block_tables_after_cow())
+        assert torch.equal(after, out)
+    assert_no_device_error(P)
+
+
+def test_long_context_split_matches_oracle_on_sampled_sequences(P):
+    w = workloads.make("long_splitk", seed=0, device=DEV)
+    slots, out = full_step(P, w)
+    assert np.array_equal(slots.cpu().numpy(),
+                          oracle.slot_mapping(w.block_tables, w.positions, w.block_size))
+    seqs = [0, int(np.argmax(w.context_lens))]
+    k, v, bt, ctx, q = compact_for_oracle(w, seqs)
+    ref = oracle.paged_decode(w.dtype, k, v, q, bt, ctx, w.scale)
+    assert max_abs(out[seqs], ref) <= TOL[w.dtype]
+    assert_no_device_error(P)
