@@ -185,6 +185,36 @@ pkv_status pkv_lse_merge(const void* workspace, size_t workspace_bytes, int32_t 
                          int32_t out_dtype, void* stream);
 
 /*
+ * Decode without a caller-provided workspace.  The pages have no counterpart
+ * to this: it exists for callers that cannot allocate device memory
+ * themselves, for example a plugin whose host engine owns every device
+ * allocation and forbids new ones while it enqueues work, or a caller reaching
+ * this library through a foreign-function layer that has no device allocator.
+ * Same arguments and result as pkv_paged_attention_decode, minus the
+ * workspace.  When the call needs partition scratch (see
+ * pkv_decode_workspace_bytes), it uses a fixed array inside libpagedkv.so of
+ * PKV_STATIC_WORKSPACE_BYTES bytes; every GPU that loads the library holds that
+ * array until the process exits.  A call that would need more returns
+ * PKV_ERR_WORKSPACE without launching anything (a larger partition_size needs
+ * less).  The call allocates nothing: no cudaMalloc, no cudaFree.
+ * The first call on a device looks the array's device address up
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.
+ * All calls share the one array and it keeps the last call's contents; the
+ * kernels write every partial result before reading it, so nothing needs
+ * clearing.  Calls whose kernels overlap on the GPU (different streams, or
+ * different host threads without ordering) race on the array and give
+ * undefined results: order them on one stream.
+ */
+#define PKV_STATIC_WORKSPACE_BYTES ((size_t)32 << 20)
+
+pkv_status pkv_paged_attention_decode_static_workspace(
+    const pkv_pool* pool, const void* q, int32_t num_seqs, int32_t num_q_heads,
+    const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* context_lens,
+    int32_t max_context_len, float scale, void* out, int32_t out_dtype, int32_t partition_size,
+    void* stream);
+
+/*
  * Copy-on-write of shared blocks: for each pair i, physical block
  * src_dst_pairs[2i+1] of both pools becomes a bit copy of block
  * src_dst_pairs[2i] (all kv heads, all rows).  "What Is vLLM", section "How

@@ -5,6 +5,7 @@
 // allocates device memory or synchronises, except pkv_get_device_error.
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "pkv_common.cuh"
 
@@ -165,6 +166,35 @@ pkv_status run_decode(const DecodeArgs& a, void* out, int32_t out_dtype, int dir
 
 }  // namespace
 
+// Partition scratch of pkv_paged_attention_decode_static_workspace, for callers
+// that cannot allocate device memory: one fixed array per device, held for the
+// life of the process, shared by every call of that entry point.
+static __device__ __align__(256) unsigned char pkv_static_workspace[PKV_STATIC_WORKSPACE_BYTES];
+
+namespace {
+
+void* g_static_ws_ptr[MAX_DEVICES] = {nullptr};
+cudaError_t g_static_ws_status[MAX_DEVICES];
+std::once_flag g_static_ws_once[MAX_DEVICES];
+
+// Device address of the array on the current device, looked up once per
+// device with that device current.  Host code only sees a stand-in for the
+// array's name, never a usable device address, so the kernels get this one.
+pkv_status static_workspace(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return PKV_ERR_CUDA;
+    std::call_once(g_static_ws_once[dev], [dev] {
+        void* ptr = nullptr;
+        g_static_ws_status[dev] = cudaGetSymbolAddress(&ptr, pkv_static_workspace);
+        g_static_ws_ptr[dev] = ptr;
+    });
+    if (g_static_ws_status[dev] != cudaSuccess || !g_static_ws_ptr[dev]) return PKV_ERR_CUDA;
+    *out = g_static_ws_ptr[dev];
+    return PKV_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 int32_t pkv_version(void) { return 100; }
@@ -258,6 +288,28 @@ pkv_status pkv_paged_attention_decode(const pkv_pool* pool, const void* q, int32
     if (num_seqs > 0 && !out) return PKV_ERR_INVALID;
     if (out_dtype != PKV_F32 && out_dtype != pool->dtype) return PKV_ERR_UNSUPPORTED;
     return run_decode(a, out, out_dtype, 1, workspace, workspace_bytes,
+                      static_cast<cudaStream_t>(stream));
+}
+
+pkv_status pkv_paged_attention_decode_static_workspace(
+    const pkv_pool* pool, const void* q, int32_t num_seqs, int32_t num_q_heads,
+    const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* context_lens,
+    int32_t max_context_len, float scale, void* out, int32_t out_dtype, int32_t partition_size,
+    void* stream) {
+    DecodeArgs a{pool, q, num_seqs, num_q_heads, block_tables, max_blocks_per_seq,
+                 context_lens, max_context_len, scale, partition_size};
+    pkv_status st = check_decode(a);
+    if (st != PKV_OK) return st;
+    if (num_seqs > 0 && !out) return PKV_ERR_INVALID;
+    if (out_dtype != PKV_F32 && out_dtype != pool->dtype) return PKV_ERR_UNSUPPORTED;
+    const size_t need = pkv_decode_workspace_bytes(pool, num_seqs, num_q_heads, max_context_len,
+                                                   partition_size);
+    if (need > PKV_STATIC_WORKSPACE_BYTES) return PKV_ERR_WORKSPACE;
+    if (num_seqs == 0) return PKV_OK;
+    void* ws = nullptr;
+    st = static_workspace(&ws);
+    if (st != PKV_OK) return st;
+    return run_decode(a, out, out_dtype, 1, ws, PKV_STATIC_WORKSPACE_BYTES,
                       static_cast<cudaStream_t>(stream));
 }
 

@@ -46,6 +46,8 @@ _SIGS = {
     "pkv_partition_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32]),
     "pkv_paged_attention_decode": (_i32, [_PP, _P, _i32, _i32, _P, _i32, _P, _i32, _f32, _P, _i32,
                                           _i32, _P, _sz, _P]),
+    "pkv_paged_attention_decode_static_workspace": (_i32, [_PP, _P, _i32, _i32, _P, _i32, _P,
+                                                           _i32, _f32, _P, _i32, _i32, _P]),
     "pkv_paged_attention_partitions": (_i32, [_PP, _P, _i32, _i32, _P, _i32, _P, _i32, _f32, _i32,
                                               _P, _sz, _P]),
     "pkv_lse_merge": (_i32, [_P, _sz, _i32, _i32, _i32, _P, _i32, _i32, _P, _i32, _P]),
@@ -162,6 +164,23 @@ def pkv_paged_attention_decode(q, k_pool, v_pool, block_tables, context_lens, sc
                                           _DTYPE[out.dtype], int(partition_size), _ptr(workspace),
                                           ws_bytes, _stream(stream, q)),
            "pkv_paged_attention_decode")
+
+
+def pkv_paged_attention_decode_static_workspace(q, k_pool, v_pool, block_tables, context_lens,
+                                                scale, out, max_context_len, partition_size=0,
+                                                stream=None):
+    """Decode for callers that cannot allocate device memory: the partition scratch is a
+    fixed array inside the library (PKV_STATIC_WORKSPACE_BYTES) shared by all calls."""
+    _contig(q, block_tables, context_lens, out)
+    pool = make_pool(k_pool, v_pool)
+    S, Hq, _ = q.shape
+    _check(lib.pkv_paged_attention_decode_static_workspace(
+        ctypes.byref(pool), _ptr(q), S, Hq, _ptr(block_tables), block_tables.shape[1],
+        _ptr(context_lens), int(max_context_len), float(scale), _ptr(out), _DTYPE[out.dtype],
+        int(partition_size), _stream(stream, q)), "pkv_paged_attention_decode_static_workspace")
+
+
+STATIC_WORKSPACE_BYTES = 32 << 20
 
 
 def pkv_paged_attention_partitions(q, k_pool, v_pool, block_tables, context_lens, scale,
