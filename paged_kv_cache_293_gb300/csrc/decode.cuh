@@ -322,8 +322,14 @@ paged_decode_kernel(const DecodeParams p) {
     }
 }
 
-// Ring shape per element type / head size: NW warps per CTA, NS stages per warp.
-template <typename T, int D> struct DecodeShape { static constexpr int NW = 4, NS = 3; };
+// Ring shape: NW warps per CTA, NS stages per warp, sized so that a CTA holds
+// 64 KB of ring and three CTAs (12 warps) fit on an SM.  Measured on the
+// LLaMA-13B batch: 4 warps x 2 stages of 8 KB beat 3-4 stages or 2 / 8 warps.
+template <typename T, int D> struct DecodeShape {
+    static constexpr int STAGE = 2 * Geometry<T, D>::CHUNK_BYTES;
+    static constexpr int NW = STAGE > 8192 ? 2 : 4;
+    static constexpr int NS = (64 * 1024) / (NW * STAGE);
+};
 
 template <typename T, int D, int G>
 cudaError_t launch_decode_tdg(const DecodeParams& p, cudaStream_t stream) {
