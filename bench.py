@@ -300,7 +300,7 @@ def run_ours(args):
     peak, peak_kind = read_peaks()
     value = world * total / (step_ms_max * 1e-3) / 1e9
     dec_gbs = dec_unique / (dec_ms * 1e-3) / 1e9
-    traffic = read_traffic(["decode.cuh", "pkv_common.cuh", "kernels_misc.cu"], args.workload)
+    traffic = read_traffic(["decode.cuh", "pkv_common.cuh"], args.workload)
 
     if rank != 0:
         return

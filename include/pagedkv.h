@@ -160,6 +160,31 @@ pkv_status pkv_paged_attention_decode(const pkv_pool* pool, const void* q, int32
                                       size_t workspace_bytes, void* stream);
 
 /*
+ * Append and decode in one launch: for every sequence s with
+ * context_lens[s] >= 1, the new token sits at position p = context_lens[s] - 1
+ * (the context includes it).  Its rows k_new[s][h], v_new[s][h] are written
+ * into slot block_tables[s][p / B] * B + p % B of both pools, and the
+ * attention over positions [0, context_lens[s]) uses them for position p.
+ * The result (output and pools) is that of pkv_slot_mapping with positions =
+ * context_lens - 1, then pkv_kv_cache_write, then pkv_paged_attention_decode,
+ * with one launch instead of three ("vLLM in Production", section
+ * "PagedAttention - Virtual Memory for the KV Cache": the cache grows as tokens
+ * arrive; each new token then attends to all cached tokens).
+ *   k_new, v_new   [num_seqs][num_kv_heads][head_dim], pool type, 16-byte aligned
+ *   slot_mapping   optional int64 [num_seqs] output: the slot written (-1 for
+ *                  an empty context or a bad table entry); NULL to skip
+ * The block receiving a new token must belong to that sequence alone (copy it
+ * on write first when it is shared).  Other arguments as in
+ * pkv_paged_attention_decode.
+ */
+pkv_status pkv_paged_attention_decode_append(
+    const pkv_pool* pool, const void* q, const void* k_new, const void* v_new, int32_t num_seqs,
+    int32_t num_q_heads, const int32_t* block_tables, int32_t max_blocks_per_seq,
+    const int32_t* context_lens, int32_t max_context_len, float scale, void* out,
+    int32_t out_dtype, int32_t partition_size, void* workspace, size_t workspace_bytes,
+    int64_t* slot_mapping, void* stream);
+
+/*
  * The partition step alone: for every sequence s, q head h and partition
  * k < ceil(context_lens[s] / partition_size), writes (m, l, o) of tokens
  * [k P, min(ctx, (k+1) P)) to the workspace in the layout above (a context
@@ -226,6 +251,27 @@ pkv_status pkv_paged_attention_decode_static_workspace(
  */
 pkv_status pkv_copy_blocks(const pkv_pool* pool, const int32_t* src_dst_pairs, int32_t num_pairs,
                            void* stream);
+
+/*
+ * Move whole blocks between two pools of the same geometry (dtype, block
+ * size, kv heads, head_dim): for each pair i, block src_dst_pairs[2i+1] of dst
+ * becomes a bit copy of block src_dst_pairs[2i] of src, K and V.  For
+ * preemption, a sequence's blocks go from the GPU pool to a pool in host
+ * memory and back later ("What Is vLLM", section "What is continuous batching
+ * in vLLM?": low-priority sequences are preempted and their KV caches swapped
+ * to CPU memory).  The copies run in a kernel that reads and writes both pools
+ * directly, so either pool may be device memory or pinned host memory the GPU
+ * can address (cudaHostAlloc / cudaMallocHost; with unified addressing its
+ * host pointer is valid on the device); src_dst_pairs (int32 [num_pairs][2])
+ * must be device-addressable too.  Every pointer is checked with
+ * cudaPointerGetAttributes first: pinned host memory is used through its mapped
+ * device address, and memory the runtime does not know (plain pageable host
+ * memory) returns PKV_ERR_INVALID.  dst blocks must be distinct and must not
+ * overlap the src blocks read in the same call.  Pairs outside either pool are
+ * skipped and set PKV_DEVERR_PAIR.
+ */
+pkv_status pkv_swap_blocks(const pkv_pool* src, const pkv_pool* dst, const int32_t* src_dst_pairs,
+                           int32_t num_pairs, void* stream);
 
 /*
  * Synchronises stream, then reads and clears the current device's error word

@@ -17,6 +17,9 @@ pages it follows and the readings it takes where the pages are silent):
 - ``kv_cache_write``    bit copy of new K/V rows into their slots.
 - ``copy_blocks``       whole-block copy for copy-on-write of shared blocks
                         (same page, "Memory sharing").
+- ``swap_blocks``       whole-block copy between two pools (device <-> host swap
+                        of preempted sequences, same page, "What is continuous
+                        batching in vLLM?").
 """
 import ctypes
 import os
@@ -50,11 +53,13 @@ def lib():
         _lib.oracle_slot_mapping.argtypes = [P, i32, P, P, i32, i32, P]
         _lib.oracle_kv_cache_write.argtypes = [ctypes.c_int, P, P, i32, i32, i32, i32, P, P, P, i32]
         _lib.oracle_copy_blocks.argtypes = [P, P, i32, i64, P, i32]
+        _lib.oracle_swap_blocks.argtypes = [P, P, i32, P, P, i32, i64, P, i32]
         _lib.oracle_convert_to_double.argtypes = [ctypes.c_int, P, i64, P]
         _lib.oracle_num_threads.restype = ctypes.c_int
         _lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
         for name in ("oracle_paged_decode", "oracle_partition_decode", "oracle_lse_merge",
-                     "oracle_slot_mapping", "oracle_kv_cache_write", "oracle_copy_blocks"):
+                     "oracle_slot_mapping", "oracle_kv_cache_write", "oracle_copy_blocks",
+                     "oracle_swap_blocks"):
             getattr(_lib, name).restype = ctypes.c_int
     return _lib
 
@@ -188,3 +193,16 @@ def copy_blocks(k_pool, v_pool, pairs):
     block_bytes = k_pool.nbytes // N
     _check(lib().oracle_copy_blocks(_ptr(k_pool), _ptr(v_pool), N, block_bytes, _ptr(pr),
                                     pr.shape[0]))
+
+
+def swap_blocks(src_k, src_v, dst_k, dst_v, pairs):
+    """Block dst of (dst_k, dst_v) <- block src of (src_k, src_v) for each (src, dst) pair."""
+    for a in (src_k, src_v, dst_k, dst_v):
+        if not a.flags.c_contiguous:
+            raise ValueError("pools must be contiguous")
+    if src_k.shape[1:] != dst_k.shape[1:] or src_k.dtype.itemsize != dst_k.dtype.itemsize:
+        raise ValueError("pools must have the same block geometry")
+    pr = np.ascontiguousarray(pairs, dtype=np.int32).reshape(-1, 2)
+    block_bytes = src_k.nbytes // src_k.shape[0]
+    _check(lib().oracle_swap_blocks(_ptr(src_k), _ptr(src_v), src_k.shape[0], _ptr(dst_k),
+                                    _ptr(dst_v), dst_k.shape[0], block_bytes, _ptr(pr), pr.shape[0]))

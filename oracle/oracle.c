@@ -394,3 +394,26 @@ int oracle_copy_blocks(void* k_pool, void* v_pool, int32_t num_blocks, int64_t b
     }
     return rc;
 }
+
+/*
+ * Swap between two pools of the same block geometry (for example the GPU pool
+ * and a pool in host memory, as when a preempted sequence's KV cache is moved
+ * to the CPU: "What Is vLLM", section "What is continuous batching in vLLM?").
+ * For each pair (src, dst): block dst of the destination pools becomes a copy
+ * of block src of the source pools, K and V.
+ */
+int oracle_swap_blocks(const void* src_k, const void* src_v, int32_t src_blocks, void* dst_k,
+                       void* dst_v, int32_t dst_blocks, int64_t block_bytes, const int32_t* pairs,
+                       int32_t num_pairs) {
+    if (src_blocks <= 0 || dst_blocks <= 0 || block_bytes <= 0 || num_pairs < 0) return ORC_ERR_ARG;
+    int rc = ORC_OK;
+    for (int32_t i = 0; i < num_pairs; ++i) {
+        int32_t src = pairs[2 * i], dst = pairs[2 * i + 1];
+        if (src < 0 || src >= src_blocks || dst < 0 || dst >= dst_blocks) { rc = ORC_ERR_BLOCK; continue; }
+        memcpy((char*)dst_k + (int64_t)dst * block_bytes, (const char*)src_k + (int64_t)src * block_bytes,
+               (size_t)block_bytes);
+        memcpy((char*)dst_v + (int64_t)dst * block_bytes, (const char*)src_v + (int64_t)src * block_bytes,
+               (size_t)block_bytes);
+    }
+    return rc;
+}

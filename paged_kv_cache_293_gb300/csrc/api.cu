@@ -102,9 +102,17 @@ cudaError_t launch_decode_typed(const pkv::DecodeParams& p, int32_t dtype, int D
     }
 }
 
-// Shared body of decode (direct = 1) and the partition step (direct = 0).
+struct AppendArgs {
+    const void* k_new;
+    const void* v_new;
+    int64_t* slot_out;
+};
+
+// Shared body of decode (direct = 1) and the partition step (direct = 0);
+// `append` (may be null) turns on the fused write of each sequence's new token.
 pkv_status run_decode(const DecodeArgs& a, void* out, int32_t out_dtype, int direct,
-                      void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                      const AppendArgs* append = nullptr) {
     const pkv_pool* pool = a.pool;
     const int32_t P = a.P > 0 ? a.P : auto_partition(pool, a.max_ctx);
     const int32_t parts = a.max_ctx > 0 ? ceil_div(a.max_ctx, P) : 1;
@@ -142,6 +150,11 @@ pkv_status run_decode(const DecodeArgs& a, void* out, int32_t out_dtype, int dir
         p.ws_m = reinterpret_cast<float*>(ws);
         p.ws_l = reinterpret_cast<float*>(ws + lay.l_off);
         p.ws_o = reinterpret_cast<float*>(ws + lay.o_off);
+    }
+    if (append) {
+        p.k_new = append->k_new;
+        p.v_new = append->v_new;
+        p.slot_out = append->slot_out;
     }
     p.err = err;
     const int G = a.Hq / pool->num_kv_heads;
@@ -316,6 +329,24 @@ pkv_status pkv_paged_attention_decode_static_workspace(
                       static_cast<cudaStream_t>(stream));
 }
 
+pkv_status pkv_paged_attention_decode_append(
+    const pkv_pool* pool, const void* q, const void* k_new, const void* v_new, int32_t num_seqs,
+    int32_t num_q_heads, const int32_t* block_tables, int32_t max_blocks_per_seq,
+    const int32_t* context_lens, int32_t max_context_len, float scale, void* out,
+    int32_t out_dtype, int32_t partition_size, void* workspace, size_t workspace_bytes,
+    int64_t* slot_mapping, void* stream) {
+    DecodeArgs a{pool, q, num_seqs, num_q_heads, block_tables, max_blocks_per_seq,
+                 context_lens, max_context_len, scale, partition_size};
+    pkv_status st = check_decode(a);
+    if (st != PKV_OK) return st;
+    if (num_seqs > 0 && (!out || !k_new || !v_new)) return PKV_ERR_INVALID;
+    if (num_seqs > 0 && (!aligned16(k_new) || !aligned16(v_new))) return PKV_ERR_INVALID;
+    if (out_dtype != PKV_F32 && out_dtype != pool->dtype) return PKV_ERR_UNSUPPORTED;
+    const AppendArgs app{k_new, v_new, slot_mapping};
+    return run_decode(a, out, out_dtype, 1, workspace, workspace_bytes,
+                      static_cast<cudaStream_t>(stream), &app);
+}
+
 pkv_status pkv_paged_attention_partitions(const pkv_pool* pool, const void* q, int32_t num_seqs,
                                           int32_t num_q_heads, const int32_t* block_tables,
                                           int32_t max_blocks_per_seq,
@@ -377,7 +408,65 @@ pkv_status pkv_copy_blocks(const pkv_pool* pool, const int32_t* src_dst_pairs, i
     unsigned int* err = nullptr;
     st = error_word(&err);
     if (st != PKV_OK) return st;
-    return pkv::launch_copy_blocks(*pool, src_dst_pairs, num_pairs, err,
+    return pkv::launch_copy_blocks(*pool, *pool, src_dst_pairs, num_pairs, err,
+                                   static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PKV_OK
+               : PKV_ERR_CUDA;
+}
+
+namespace {
+
+// Device address of a pointer the kernels will dereference: device and managed
+// memory as they are, pinned host memory through its mapped device address.
+// Pageable host memory the runtime does not know is refused rather than risked.
+bool device_addressable(const void* p, const void** out) {
+    cudaPointerAttributes attr{};
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    switch (attr.type) {
+        case cudaMemoryTypeDevice:
+        case cudaMemoryTypeManaged:
+            *out = p;
+            return true;
+        case cudaMemoryTypeHost:
+            *out = attr.devicePointer;
+            return attr.devicePointer != nullptr;
+        default:
+            return false;
+    }
+}
+
+}  // namespace
+
+pkv_status pkv_swap_blocks(const pkv_pool* src, const pkv_pool* dst, const int32_t* src_dst_pairs,
+                           int32_t num_pairs, void* stream) {
+    pkv_status st = check_pool(src);
+    if (st != PKV_OK) return st;
+    st = check_pool(dst);
+    if (st != PKV_OK) return st;
+    if (src->dtype != dst->dtype || src->block_size != dst->block_size ||
+        src->num_kv_heads != dst->num_kv_heads || src->head_dim != dst->head_dim)
+        return PKV_ERR_INVALID;
+    if (num_pairs < 0) return PKV_ERR_INVALID;
+    if (num_pairs == 0) return PKV_OK;
+    if (!src_dst_pairs) return PKV_ERR_INVALID;
+    pkv_pool s2 = *src, d2 = *dst;
+    const void* pairs = nullptr;
+    const void *sk, *sv, *dk, *dv;
+    if (!device_addressable(src->k, &sk) || !device_addressable(src->v, &sv) ||
+        !device_addressable(dst->k, &dk) || !device_addressable(dst->v, &dv) ||
+        !device_addressable(src_dst_pairs, &pairs))
+        return PKV_ERR_INVALID;
+    s2.k = const_cast<void*>(sk);
+    s2.v = const_cast<void*>(sv);
+    d2.k = const_cast<void*>(dk);
+    d2.v = const_cast<void*>(dv);
+    unsigned int* err = nullptr;
+    st = error_word(&err);
+    if (st != PKV_OK) return st;
+    return pkv::launch_copy_blocks(s2, d2, static_cast<const int32_t*>(pairs), num_pairs, err,
                                    static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? PKV_OK
                : PKV_ERR_CUDA;

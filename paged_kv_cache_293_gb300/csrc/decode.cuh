@@ -87,6 +87,7 @@ paged_decode_kernel(const DecodeParams p) {
     const int B = p.block_size, Hkv = p.num_kv_heads, Hq = p.num_q_heads, P = p.partition_size;
 
     int ctx = p.context_lens[s];
+    bool ctx_bad = false;
     {
         const long long cap_table = (long long)p.max_blocks_per_seq * B;
         const long long cap_grid = (long long)p.max_parts * P;
@@ -95,6 +96,7 @@ paged_decode_kernel(const DecodeParams p) {
         if (ctx < 0 || ctx > cap) {
             if (threadIdx.x == 0 && part == 0 && kvh == 0) set_error(p.err, PKV_DEVERR_CONTEXT);
             ctx = ctx < 0 ? 0 : int(cap);
+            ctx_bad = true;
         }
     }
     const int n_parts = (ctx + P - 1) / P;
@@ -102,6 +104,8 @@ paged_decode_kernel(const DecodeParams p) {
     if (part > 0 && tok0 >= ctx) return;
     const bool direct = p.direct_single && n_parts <= 1;
 
+    if ((ctx == 0 || ctx_bad) && p.slot_out && kvh == 0 && part == 0 && threadIdx.x == 0)
+        p.slot_out[s] = -1;
     if (ctx == 0) {  // only part 0 gets here: zero output or an empty partial
         for (int i = threadIdx.x; i < G * D; i += NW * 32) {
             const int h = kvh * G + i / D, d = i % D;
@@ -145,6 +149,23 @@ paged_decode_kernel(const DecodeParams p) {
     __syncwarp();
 
     const int32_t* bt_row = p.block_tables + (size_t)s * p.max_blocks_per_seq;
+
+    // ---- fused append: the partition holding position ctx - 1 writes the new K/V rows
+    // of its kv head into their slot and splices them into the staged chunk.
+    const int p_new = ctx - 1;
+    const bool has_new = p.k_new != nullptr && !ctx_bad && p_new >= tok0 && p_new < tok_end;
+    const int c_new = has_new ? (p_new - tok0) / CHUNK_TOKENS : -1;
+    const bool warp_new = has_new && (c_new % NW) == warp;
+    uint4 k_row = make_uint4(0, 0, 0, 0), v_row = make_uint4(0, 0, 0, 0);
+    int phys_new = -1;
+    if (warp_new) {
+        phys_new = __ldg(bt_row + p_new / B);
+        if (lane < CPR) {
+            const size_t src = ((size_t)s * Hkv + kvh) * D;
+            k_row = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.k_new) + src) + lane);
+            v_row = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.v_new) + src) + lane);
+        }
+    }
     const T* kbase = static_cast<const T*>(p.k_pool);
     const T* vbase = static_cast<const T*>(p.v_pool);
     const uint64_t policy = l2_evict_first_policy();
@@ -206,6 +227,21 @@ paged_decode_kernel(const DecodeParams p) {
         }
         const int c = warp + NW * i;
         const int valid = min(CHUNK_TOKENS, tok_end - (tok0 + c * CHUNK_TOKENS));
+        if (warp_new && c == c_new) {
+            const bool ok = (unsigned)phys_new < (unsigned)p.num_blocks;
+            if (ok && lane < CPR) {
+                unsigned char* Kw = ring + st * Smem::STAGE_BYTES;
+                const int r = (p_new - tok0) & (CHUNK_TOKENS - 1);
+                *reinterpret_cast<uint4*>(Kw + r * ROWB + lane * 16) = k_row;
+                *reinterpret_cast<uint4*>(Kw + CHB + r * ROWB + lane * 16) = v_row;
+                const size_t off = (((size_t)phys_new * Hkv + kvh) * B + (p_new % B)) * D;
+                reinterpret_cast<uint4*>(const_cast<T*>(kbase) + off)[lane] = k_row;
+                reinterpret_cast<uint4*>(const_cast<T*>(vbase) + off)[lane] = v_row;
+            }
+            if (p.slot_out && kvh == 0 && lane == 0)
+                p.slot_out[s] = ok ? (int64_t)phys_new * B + (p_new % B) : -1;
+            __syncwarp();
+        }
         if (!((bad_stages >> st) & 1)) {
             const unsigned char* Ks = ring + st * Smem::STAGE_BYTES;
             const unsigned char* Vs = Ks + CHB;

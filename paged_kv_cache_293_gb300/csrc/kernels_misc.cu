@@ -89,37 +89,41 @@ cudaError_t launch_cache_write(const pkv_pool& pool, const void* k_new, const vo
     return cudaGetLastError();
 }
 
-// ------------------------------------------------------------------ copy-on-write block copy
-// "What Is vLLM", section "How does PagedAttention work?", step "Memory sharing".
-// grid = (pairs, slices of a block, 2 pools); 16-byte vectors.
-__global__ void copy_blocks_kernel(uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
-                                   int32_t num_blocks, long long vec_per_block,
+// ------------------------------------------------------------------ block copy between pools
+// Copy-on-write inside one pool ("What Is vLLM", section "How does PagedAttention
+// work?", step "Memory sharing") and swapping between a device pool and a pool in
+// pinned host memory (same page, "What is continuous batching in vLLM?": preempted
+// sequences' KV caches move to the CPU).  grid = (pairs, slices of a block, 2 pools);
+// 16-byte vectors.
+__global__ void copy_blocks_kernel(const uint4* __restrict__ src_k, const uint4* __restrict__ src_v,
+                                   uint4* __restrict__ dst_k, uint4* __restrict__ dst_v,
+                                   int32_t src_blocks, int32_t dst_blocks, long long vec_per_block,
                                    const int32_t* __restrict__ pairs, unsigned int* err) {
     const int i = blockIdx.x;
     const int src = pairs[2 * i], dst = pairs[2 * i + 1];
-    if ((unsigned)src >= (unsigned)num_blocks || (unsigned)dst >= (unsigned)num_blocks) {
+    if ((unsigned)src >= (unsigned)src_blocks || (unsigned)dst >= (unsigned)dst_blocks) {
         if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) set_error(err, PKV_DEVERR_PAIR);
         return;
     }
-    uint4* pool = blockIdx.z == 0 ? k_pool : v_pool;
-    const uint4* from = pool + (size_t)src * vec_per_block;
-    uint4* to = pool + (size_t)dst * vec_per_block;
+    const uint4* from = (blockIdx.z == 0 ? src_k : src_v) + (size_t)src * vec_per_block;
+    uint4* to = (blockIdx.z == 0 ? dst_k : dst_v) + (size_t)dst * vec_per_block;
     for (long long j = (long long)blockIdx.y * blockDim.x + threadIdx.x; j < vec_per_block;
          j += (long long)gridDim.y * blockDim.x)
         to[j] = from[j];
 }
 
-cudaError_t launch_copy_blocks(const pkv_pool& pool, const int32_t* pairs, int32_t num_pairs,
-                               unsigned int* err, cudaStream_t stream) {
-    const long long vec = (long long)pool.num_kv_heads * pool.block_size * pool.head_dim *
-                          elem_bytes(pool.dtype) / 16;
+cudaError_t launch_copy_blocks(const pkv_pool& src, const pkv_pool& dst, const int32_t* pairs,
+                               int32_t num_pairs, unsigned int* err, cudaStream_t stream) {
+    const long long vec = (long long)src.num_kv_heads * src.block_size * src.head_dim *
+                          elem_bytes(src.dtype) / 16;
     const int threads = 256;
     long long slices = (vec + threads * 4 - 1) / (threads * 4);
     if (slices > 65535) slices = 65535;
     dim3 grid((unsigned)num_pairs, (unsigned)slices, 2);
-    copy_blocks_kernel<<<grid, threads, 0, stream>>>(static_cast<uint4*>(pool.k),
-                                                     static_cast<uint4*>(pool.v), pool.num_blocks,
-                                                     vec, pairs, err);
+    copy_blocks_kernel<<<grid, threads, 0, stream>>>(
+        static_cast<const uint4*>(src.k), static_cast<const uint4*>(src.v),
+        static_cast<uint4*>(dst.k), static_cast<uint4*>(dst.v), src.num_blocks, dst.num_blocks,
+        vec, pairs, err);
     return cudaGetLastError();
 }
 

@@ -42,6 +42,12 @@ struct DecodeParams {
     float* ws_m;
     float* ws_l;
     float* ws_o;
+    // Fused append (null when off): the new token of sequence s sits at position
+    // context_lens[s] - 1; its K/V rows k_new[s], v_new[s] ([S][Hkv][D]) are written
+    // into that slot of the pools and used in place of the rows read from them.
+    const void* k_new;
+    const void* v_new;
+    int64_t* slot_out;      // optional: the slot each new token went to (-1: none)
     unsigned int* err;
 };
 
@@ -204,7 +210,7 @@ cudaError_t launch_slot_mapping(const int32_t* block_tables, int32_t max_blocks_
 cudaError_t launch_cache_write(const pkv_pool& pool, const void* k_new, const void* v_new,
                                const int64_t* slot_mapping, int32_t num_tokens, unsigned int* err,
                                cudaStream_t stream);
-cudaError_t launch_copy_blocks(const pkv_pool& pool, const int32_t* pairs, int32_t num_pairs,
-                               unsigned int* err, cudaStream_t stream);
+cudaError_t launch_copy_blocks(const pkv_pool& src, const pkv_pool& dst, const int32_t* pairs,
+                               int32_t num_pairs, unsigned int* err, cudaStream_t stream);
 
 }  // namespace pkv

@@ -48,10 +48,13 @@ _SIGS = {
                                           _i32, _P, _sz, _P]),
     "pkv_paged_attention_decode_static_workspace": (_i32, [_PP, _P, _i32, _i32, _P, _i32, _P,
                                                            _i32, _f32, _P, _i32, _i32, _P]),
+    "pkv_paged_attention_decode_append": (_i32, [_PP, _P, _P, _P, _i32, _i32, _P, _i32, _P, _i32,
+                                                 _f32, _P, _i32, _i32, _P, _sz, _P, _P]),
     "pkv_paged_attention_partitions": (_i32, [_PP, _P, _i32, _i32, _P, _i32, _P, _i32, _f32, _i32,
                                               _P, _sz, _P]),
     "pkv_lse_merge": (_i32, [_P, _sz, _i32, _i32, _i32, _P, _i32, _i32, _P, _i32, _P]),
     "pkv_copy_blocks": (_i32, [_PP, _P, _i32, _P]),
+    "pkv_swap_blocks": (_i32, [_PP, _PP, _P, _i32, _P]),
     "pkv_get_device_error": (_i32, [ctypes.POINTER(ctypes.c_uint32), _P]),
     "pkv_status_str": (ctypes.c_char_p, [_i32]),
     "pkv_version": (_i32, []),
@@ -166,6 +169,21 @@ def pkv_paged_attention_decode(q, k_pool, v_pool, block_tables, context_lens, sc
            "pkv_paged_attention_decode")
 
 
+def pkv_paged_attention_decode_append(q, k_pool, v_pool, k_new, v_new, block_tables,
+                                      context_lens, scale, out, max_context_len,
+                                      partition_size=0, workspace=None, slot_mapping=None,
+                                      stream=None):
+    _contig(q, k_new, v_new, block_tables, context_lens, out, workspace, slot_mapping)
+    pool = make_pool(k_pool, v_pool)
+    S, Hq, _ = q.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.pkv_paged_attention_decode_append(
+        ctypes.byref(pool), _ptr(q), _ptr(k_new), _ptr(v_new), S, Hq, _ptr(block_tables),
+        block_tables.shape[1], _ptr(context_lens), int(max_context_len), float(scale), _ptr(out),
+        _DTYPE[out.dtype], int(partition_size), _ptr(workspace), ws_bytes, _ptr(slot_mapping),
+        _stream(stream, q)), "pkv_paged_attention_decode_append")
+
+
 def pkv_paged_attention_decode_static_workspace(q, k_pool, v_pool, block_tables, context_lens,
                                                 scale, out, max_context_len, partition_size=0,
                                                 stream=None):
@@ -212,6 +230,17 @@ def pkv_copy_blocks(k_pool, v_pool, src_dst_pairs, stream=None):
     n = src_dst_pairs.numel() // 2
     _check(lib.pkv_copy_blocks(ctypes.byref(pool), _ptr(src_dst_pairs), n, _stream(stream, k_pool)),
            "pkv_copy_blocks")
+
+
+def pkv_swap_blocks(src_k, src_v, dst_k, dst_v, src_dst_pairs, stream=None):
+    """Blocks between two pools (device or pinned host tensors); pairs on the device or pinned."""
+    _contig(src_dst_pairs)
+    src = make_pool(src_k, src_v)
+    dst = make_pool(dst_k, dst_v)
+    ref = src_k if src_k.is_cuda else dst_k
+    n = src_dst_pairs.numel() // 2
+    _check(lib.pkv_swap_blocks(ctypes.byref(src), ctypes.byref(dst), _ptr(src_dst_pairs), n,
+                               _stream(stream, ref)), "pkv_swap_blocks")
 
 
 def pkv_get_device_error(stream=None, device=None):

@@ -307,3 +307,77 @@ def test_long_context_split_matches_oracle_on_sampled_sequences(P):
     ref = oracle.paged_decode(w.dtype, k, v, q, bt, ctx, w.scale)
     assert max_abs(out[seqs], ref) <= TOL[w.dtype]
     assert_no_device_error(P)
+
+
+# ------------------------------------------------------------------ fused append + decode
+
+@pytest.mark.parametrize("dtype,Hq,Hkv,D,B,ctx,psize", [
+    ("f16", 8, 8, 128, 16, [1, 16, 17, 300, 1025, 0], 0),
+    ("bf16", 32, 8, 128, 32, [33, 64, 2000, 5], 512),
+    ("f32", 4, 4, 64, 16, [1, 17, 50, 100], 0),
+    ("f16", 16, 2, 64, 16, [700, 31, 4096], 256),
+])
+def test_fused_append_decode_equals_write_then_decode(P, dtype, Hq, Hkv, D, B, ctx, psize):
+    w = workloads.build("fused", dtype=dtype, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                        block_size=B, context_lens=ctx, seed=31, device=DEV)
+    k0, v0 = w.k_pool.clone(), w.v_pool.clone()
+    mcl = w.max_context_len
+    bt, cl = dev_i32(w.block_tables), dev_i32(w.context_lens)
+    ws_bytes = P.pkv_decode_workspace_bytes(w.k_pool, w.num_seqs, w.num_q_heads, mcl, psize)
+    ws = P.workspace_tensor(ws_bytes, DEV) if ws_bytes else None
+    out = torch.full((w.num_seqs, Hq, D), float("nan"), dtype=torch.float32, device=DEV)
+    slots = torch.full((w.num_seqs,), -7, dtype=torch.int64, device=DEV)
+    P.pkv_paged_attention_decode_append(w.q, w.k_pool, w.v_pool, w.k_new, w.v_new, bt, cl,
+                                        w.scale, out, mcl, psize, ws, slot_mapping=slots)
+    torch.cuda.synchronize()
+    # oracle: slot mapping, write, decode
+    ref_slots = oracle.slot_mapping(w.block_tables, w.positions, B)
+    assert np.array_equal(slots.cpu().numpy(), ref_slots)
+    kr, vr = host(k0).copy(), host(v0).copy()
+    oracle.kv_cache_write(dtype, kr, vr, host(w.k_new), host(w.v_new), ref_slots)
+    assert np.array_equal(host(w.k_pool), kr) and np.array_equal(host(w.v_pool), vr)
+    ref = oracle.paged_decode(dtype, kr, vr, host(w.q), w.block_tables, w.context_lens, w.scale)
+    assert max_abs(out, ref) <= TOL[dtype]
+    # and bit-identical to the three-launch path on the GPU
+    w.k_pool, w.v_pool = k0, v0
+    s2 = torch.empty(w.num_seqs, dtype=torch.int64, device=DEV)
+    P.pkv_slot_mapping(bt, dev_i32(w.positions), B, s2)
+    P.pkv_kv_cache_write(w.k_pool, w.v_pool, w.k_new, w.v_new, s2)
+    out2 = run_decode(P, w, partition_size=psize)
+    assert torch.equal(out, out2)
+    assert_no_device_error(P)
+
+
+# ------------------------------------------------------------------ swap to host and back
+
+def test_swap_blocks_to_pinned_host_and_back(P):
+    w = workloads.build("swapg", dtype="bf16", num_q_heads=32, num_kv_heads=8, head_dim=128,
+                        block_size=16, context_lens=[300, 1000, 45], seed=13, device=DEV,
+                        num_blocks=200)
+    before = run_decode(P, w, partition_size=0)
+    seq, nb = 1, 63
+    used = w.block_tables[seq, :nb].copy()
+    hk = torch.zeros((nb + 5,) + tuple(w.k_pool.shape[1:]), dtype=w.k_pool.dtype).pin_memory()
+    hv = torch.zeros_like(hk).pin_memory()
+    out_pairs = np.stack([used, np.arange(nb) + 2], 1).astype(np.int32)
+    P.pkv_swap_blocks(w.k_pool, w.v_pool, hk, hv, dev_i32(out_pairs))
+    torch.cuda.synchronize()
+    rk, rv = host(hk).copy() * 0, host(hv).copy() * 0
+    oracle.swap_blocks(host(w.k_pool), host(w.v_pool), rk, rv, out_pairs)
+    assert np.array_equal(host(hk), rk) and np.array_equal(host(hv), rv)
+    # the preempted sequence's blocks are reused, then it is swapped back into other blocks
+    w.k_pool[torch.as_tensor(used, device=DEV).long()] = 0
+    w.v_pool[torch.as_tensor(used, device=DEV).long()] = 0
+    free = np.setdiff1d(np.arange(w.num_blocks), w.block_tables[w.block_tables >= 0])[:nb]
+    in_pairs = np.stack([np.arange(nb) + 2, free], 1).astype(np.int32)
+    pairs_pinned = torch.from_numpy(in_pairs).pin_memory()      # pairs may live on the host too
+    P.pkv_swap_blocks(hk, hv, w.k_pool, w.v_pool, pairs_pinned)
+    torch.cuda.synchronize()
+    bt = w.block_tables.copy()
+    bt[seq, :nb] = free
+    after = run_decode(P, w, partition_size=0, block_tables=bt)
+    assert torch.equal(before, after)
+    assert_no_device_error(P)
+    with pytest.raises(P.PagedKVError):                        # pageable host memory is refused
+        P.pkv_swap_blocks(w.k_pool, w.v_pool, torch.zeros_like(hk), torch.zeros_like(hv),
+                          dev_i32(out_pairs))

@@ -40,6 +40,9 @@ MUTANTS = [
      "int64_t blk = slot / block_size, row = slot / block_size;"),
     ("copy skips the V pool",
      "memcpy((char*)v_pool + (int64_t)dst", "if (0) memcpy((char*)v_pool + (int64_t)dst"),
+    ("swap copies K into V",
+     "memcpy((char*)dst_v + (int64_t)dst * block_bytes, (const char*)src_v",
+     "memcpy((char*)dst_v + (int64_t)dst * block_bytes, (const char*)src_k"),
     ("q rows read head-major",
      "qd[d] = load_as_double(q, dtype, ((int64_t)s * Hq + h) * D + d);\n            if (ctx == 0)",
      "qd[d] = load_as_double(q, dtype, ((int64_t)h * num_seqs + s) * D + d);\n            if (ctx == 0)"),

@@ -396,3 +396,32 @@ def test_out_of_pool_block_is_an_error():
     with pytest.raises(oracle.OracleError):
         oracle.paged_decode("f32", k, k, np.zeros((1, 1, 64), np.float32),
                             np.array([[3]], np.int32), [5], 1.0)
+
+
+def test_swap_out_and_back_in_restores_the_pool():
+    """Moving blocks to a second (host) pool and back into fresh blocks, then pointing the
+    table at them, leaves decode unchanged; with one pool it is the block copy."""
+    w = workloads.build("swap", dtype="f16", num_q_heads=4, num_kv_heads=2, head_dim=64,
+                        block_size=16, context_lens=[40, 70], seed=12, num_blocks=20)
+    k = workloads.storage_numpy(w.k_pool).copy()
+    v = workloads.storage_numpy(w.v_pool).copy()
+    q = workloads.storage_numpy(w.q)
+    before = oracle.paged_decode("f16", k, v, q, w.block_tables, w.context_lens, w.scale)
+    used = w.block_tables[1, :5]
+    hk = np.zeros((8,) + k.shape[1:], k.dtype)
+    hv = np.zeros_like(hk)
+    oracle.swap_blocks(k, v, hk, hv, np.stack([used, np.arange(5)], 1))
+    assert np.array_equal(hk[:5], k[used]) and np.array_equal(hv[:5], v[used])
+    free = np.setdiff1d(np.arange(20), w.block_tables[w.block_tables >= 0])[:5]
+    k[used] = 0
+    v[used] = 0
+    oracle.swap_blocks(hk, hv, k, v, np.stack([np.arange(5), free], 1))
+    bt = w.block_tables.copy()
+    bt[1, :5] = free
+    after = oracle.paged_decode("f16", k, v, q, bt, w.context_lens, w.scale)
+    assert np.array_equal(before, after)
+    k1, v1 = k.copy(), v.copy()
+    pairs = np.array([[free[0], used[0]], [free[1], used[1]]], np.int32)
+    oracle.copy_blocks(k, v, pairs)
+    oracle.swap_blocks(k1.copy(), v1.copy(), k1, v1, pairs)
+    assert np.array_equal(k, k1) and np.array_equal(v, v1)
