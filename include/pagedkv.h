@@ -185,6 +185,32 @@ pkv_status pkv_paged_attention_decode_append(
     int64_t* slot_mapping, void* stream);
 
 /*
+ * Attention for several new tokens per sequence (the tail of a chunked prefill
+ * or the draft tokens of speculative decoding: "Serving models with vLLM",
+ * section "How it works: inference serving with vLLM", names both; "How it
+ * works: continuous batching" describes chunked prefill).  The last
+ * num_queries positions of sequence s are its new tokens, already written to
+ * the cache (pkv_kv_cache_write with token_seq slots); query j (0-based)
+ * attends causally to positions [0, context_lens[s] - num_queries + j]:
+ *   out[s][j][h] = softmax(scale * q[s][j][h] . K_s[0..c_j)^T) V_s[0..c_j),
+ *   c_j = context_lens[s] - num_queries + 1 + j   (a row with c_j <= 0 is zero).
+ *   q, out   [num_seqs][num_queries][num_q_heads][head_dim]
+ * fp16 / bf16 pools only (PKV_ERR_UNSUPPORTED for fp32); always the
+ * tensor-core kernel, whose 8 columns hold (query, q head) pairs of one kv
+ * head: 8 / G queries share one pass over the pages, and more queries take
+ * further passes.  The workspace (when partitioned) is that of
+ * pkv_decode_workspace_bytes(pool, num_seqs * num_queries, num_q_heads, ...),
+ * its rows ordered [num_seqs][num_queries][num_q_heads].  Other arguments as
+ * in pkv_paged_attention_decode.
+ */
+pkv_status pkv_paged_attention_decode_multi(
+    const pkv_pool* pool, const void* q, int32_t num_queries, int32_t num_seqs,
+    int32_t num_q_heads, const int32_t* block_tables, int32_t max_blocks_per_seq,
+    const int32_t* context_lens, int32_t max_context_len, float scale, void* out,
+    int32_t out_dtype, int32_t partition_size, void* workspace, size_t workspace_bytes,
+    void* stream);
+
+/*
  * The partition step alone: for every sequence s, q head h and partition
  * k < ceil(context_lens[s] / partition_size), writes (m, l, o) of tokens
  * [k P, min(ctx, (k+1) P)) to the workspace in the layout above (a context
@@ -278,6 +304,23 @@ pkv_status pkv_swap_blocks(const pkv_pool* src, const pkv_pool* dst, const int32
  * into *flags (host pointer).  Returns PKV_ERR_DEVICE when any bit was set.
  */
 pkv_status pkv_get_device_error(uint32_t* flags, void* stream);
+
+/*
+ * Which decode kernel serves fp16 / bf16 pools (process-wide; fp32 pools always
+ * use the CUDA-core kernel):
+ *   PKV_ENGINE_AUTO          tensor cores (mma.sync, TMA-staged pages) when a kv
+ *                            head serves >= 4 q heads, CUDA cores otherwise
+ *   PKV_ENGINE_CUDA_CORES    always the CUDA-core kernel
+ *   PKV_ENGINE_TENSOR_CORES  always the tensor-core kernel (q heads padded to 8)
+ * Both give the same result within rounding; the choice is about speed.  A
+ * pool of 2^31 or more rows (num_blocks * num_kv_heads * block_size) always
+ * uses the CUDA-core kernel.  Returns PKV_ERR_INVALID for another value.
+ */
+#define PKV_ENGINE_AUTO 0
+#define PKV_ENGINE_CUDA_CORES 1
+#define PKV_ENGINE_TENSOR_CORES 2
+pkv_status pkv_set_decode_engine(int32_t engine);
+int32_t pkv_get_decode_engine(void);
 
 /* Static text for a status code. */
 const char* pkv_status_str(pkv_status status);

@@ -13,6 +13,9 @@ pages it follows and the readings it takes where the pages are silent):
                         ("What Is vLLM", section "How does PagedAttention work?").
 - ``partition_decode``  the same over ranges of P tokens, giving (m, l, o) per range.
 - ``lse_merge``         the log-sum-exp combination of such partial results.
+- ``paged_decode_multi`` several new tokens per sequence, each attending causally
+                        to the cache up to itself ("Serving models with vLLM":
+                        chunked prefill, speculative decoding).
 - ``slot_mapping``      slot = table[s][p // B] * B + p % B.
 - ``kv_cache_write``    bit copy of new K/V rows into their slots.
 - ``copy_blocks``       whole-block copy for copy-on-write of shared blocks
@@ -54,12 +57,14 @@ def lib():
         _lib.oracle_kv_cache_write.argtypes = [ctypes.c_int, P, P, i32, i32, i32, i32, P, P, P, i32]
         _lib.oracle_copy_blocks.argtypes = [P, P, i32, i64, P, i32]
         _lib.oracle_swap_blocks.argtypes = [P, P, i32, P, P, i32, i64, P, i32]
+        _lib.oracle_paged_decode_multi.argtypes = [ctypes.c_int, P, P, i32, i32, i32, i32, P, i32,
+                                                   i32, i32, P, i32, P, f32, P]
         _lib.oracle_convert_to_double.argtypes = [ctypes.c_int, P, i64, P]
         _lib.oracle_num_threads.restype = ctypes.c_int
         _lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
         for name in ("oracle_paged_decode", "oracle_partition_decode", "oracle_lse_merge",
                      "oracle_slot_mapping", "oracle_kv_cache_write", "oracle_copy_blocks",
-                     "oracle_swap_blocks"):
+                     "oracle_swap_blocks", "oracle_paged_decode_multi"):
             getattr(_lib, name).restype = ctypes.c_int
     return _lib
 
@@ -206,3 +211,19 @@ def swap_blocks(src_k, src_v, dst_k, dst_v, pairs):
     block_bytes = src_k.nbytes // src_k.shape[0]
     _check(lib().oracle_swap_blocks(_ptr(src_k), _ptr(src_v), src_k.shape[0], _ptr(dst_k),
                                     _ptr(dst_v), dst_k.shape[0], block_bytes, _ptr(pr), pr.shape[0]))
+
+
+def paged_decode_multi(dtype, k_pool, v_pool, q, block_tables, context_lens, scale):
+    """q: [S][nq][Hq][D]; the last nq positions are the new tokens; returns [S][nq][Hq][D]."""
+    code = _code(dtype)
+    e = _ELEM_BYTES[code]
+    k_pool, v_pool, q = _raw(k_pool, e), _raw(v_pool, e), _raw(q, e)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    ctx = np.ascontiguousarray(context_lens, dtype=np.int32)
+    N, Hkv, B, D = k_pool.shape
+    S, nq, Hq, _ = q.shape
+    out = np.zeros((S, nq, Hq, D), dtype=np.float64)
+    _check(lib().oracle_paged_decode_multi(code, _ptr(k_pool), _ptr(v_pool), N, B, Hkv, D, _ptr(q),
+                                           S, nq, Hq, _ptr(bt), bt.shape[1], _ptr(ctx),
+                                           float(np.float32(scale)), _ptr(out)))
+    return out

@@ -417,3 +417,76 @@ int oracle_swap_blocks(const void* src_k, const void* src_v, int32_t src_blocks,
     }
     return rc;
 }
+
+/*
+ * Several new tokens per sequence (a chunked-prefill tail or speculative draft
+ * tokens; "Serving models with vLLM", section "How it works: inference serving
+ * with vLLM").  The last nq positions of sequence s are its new tokens; query j
+ * sees positions [0, c_j) with c_j = context_lens[s] - nq + 1 + j, the causal
+ * prefix up to and including itself, and its output is the plain attention over
+ * those positions (zero when c_j <= 0).  q and out are [S][nq][Hq][D].
+ */
+int oracle_paged_decode_multi(int dtype, const void* k_pool, const void* v_pool,
+                              int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                              int32_t head_dim, const void* q, int32_t num_seqs, int32_t nq,
+                              int32_t num_q_heads, const int32_t* block_tables,
+                              int32_t max_blocks_per_seq, const int32_t* context_lens,
+                              float scale, double* out) {
+    const int32_t B = block_size, Hkv = num_kv_heads, D = head_dim, Hq = num_q_heads;
+    int rc = check_common(dtype, num_blocks, B, Hkv, D, num_seqs, Hq, max_blocks_per_seq);
+    if (rc) return rc;
+    if (nq <= 0) return ORC_ERR_ARG;
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        int32_t ctx = context_lens[s];
+        if (ctx < 0 || (int64_t)ctx > (int64_t)max_blocks_per_seq * B) return ORC_ERR_ARG;
+    }
+    const int32_t G = Hq / Hkv;
+    int err = ORC_OK;
+    int64_t units = (int64_t)num_seqs * Hkv;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t u = 0; u < units; ++u) {
+        int32_t s = (int32_t)(u / Hkv), g = (int32_t)(u % Hkv);
+        int32_t ctx = context_lens[s];
+        double* Kc = (double*)malloc(sizeof(double) * ((size_t)ctx * D + 1));
+        double* Vc = (double*)malloc(sizeof(double) * ((size_t)ctx * D + 1));
+        double* x = (double*)malloc(sizeof(double) * ((size_t)ctx + 1));
+        double* qd = (double*)malloc(sizeof(double) * (size_t)D);
+        if (!Kc || !Vc || !x || !qd) {
+#pragma omp atomic write
+            err = ORC_ERR_NOMEM;
+            free(Kc); free(Vc); free(x); free(qd);
+            continue;
+        }
+        int grc = gather_sequence(dtype, k_pool, v_pool, num_blocks, B, Hkv, D,
+                                  block_tables + (int64_t)s * max_blocks_per_seq, ctx, g, Kc, Vc);
+        if (grc) {
+#pragma omp atomic write
+            err = grc;
+        }
+        for (int32_t j = 0; j < nq && !grc; ++j) {
+            int32_t c = ctx - nq + 1 + j;
+            for (int32_t hh = 0; hh < G; ++hh) {
+                int32_t h = g * G + hh;
+                int64_t row = ((int64_t)s * nq + j) * Hq + h;
+                double* o = out + row * D;
+                if (c <= 0) {
+                    for (int32_t d = 0; d < D; ++d) o[d] = 0.0;
+                    continue;
+                }
+                for (int32_t d = 0; d < D; ++d) qd[d] = load_as_double(q, dtype, row * D + d);
+                scores(qd, Kc, 0, c, D, (double)scale, x);
+                double m = x[0];
+                for (int32_t i = 1; i < c; ++i) if (x[i] > m) m = x[i];
+                double den = 0.0;
+                for (int32_t i = 0; i < c; ++i) { x[i] = exp(x[i] - m); den += x[i]; }
+                for (int32_t d = 0; d < D; ++d) {
+                    double acc = 0.0;
+                    for (int32_t i = 0; i < c; ++i) acc += x[i] * Vc[(int64_t)i * D + d];
+                    o[d] = acc / den;
+                }
+            }
+        }
+        free(Kc); free(Vc); free(x); free(qd);
+    }
+    return err;
+}

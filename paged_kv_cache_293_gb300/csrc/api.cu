@@ -3,6 +3,8 @@
 // Host-side argument checks, the choice of partition size, workspace layout,
 // dispatch to the typed kernels, and the device error word.  Nothing here
 // allocates device memory or synchronises, except pkv_get_device_error.
+#include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -28,6 +30,8 @@ pkv_status error_word(unsigned int** out) {
     *out = g_error_ptr[dev];
     return PKV_OK;
 }
+
+std::atomic<int> g_engine{PKV_ENGINE_AUTO};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -56,13 +60,16 @@ WsLayout ws_layout(int32_t S, int32_t Hq, int32_t D, int32_t parts) {
     return WsLayout{a, 2 * a, 2 * a + rows * D * 4};
 }
 
-// One pass up to 1024 tokens; longer contexts are cut into 1024-token
-// partitions (a multiple of 16 and 32), the best of 256..8192 measured on the
-// LLaMA-7B / 13B and GQA batches.
+// One pass while the longest context is at most 3072 tokens; beyond that,
+// 1024-token partitions (a multiple of 16 and 32).  Measured on the batches
+// here: one pass was best for the LLaMA-7B (max 2048) and shared-prefix GQA
+// (max 2560) batches, 1024-token partitions for LLaMA-13B (max 4096, a long
+// lognormal tail) and the 32k-128k contexts.
 int32_t auto_partition(const pkv_pool* pool, int32_t max_context_len) {
     const int32_t B = pool->block_size;
-    const int32_t split = 1024;
-    if (max_context_len <= split) return max_context_len <= 0 ? B : ceil_div(max_context_len, B) * B;
+    const int32_t one_pass_limit = 3072, split = 1024;
+    if (max_context_len <= one_pass_limit)
+        return max_context_len <= 0 ? B : ceil_div(max_context_len, B) * B;
     return split;
 }
 
@@ -76,6 +83,7 @@ struct DecodeArgs {
     int32_t max_ctx;
     float scale;
     int32_t P;  // 0 = auto
+    int32_t NQ = 1;  // query rows per sequence
 };
 
 pkv_status check_decode(const DecodeArgs& a) {
@@ -118,7 +126,7 @@ pkv_status run_decode(const DecodeArgs& a, void* out, int32_t out_dtype, int dir
     const int32_t parts = a.max_ctx > 0 ? ceil_div(a.max_ctx, P) : 1;
     if (parts > 65535) return PKV_ERR_UNSUPPORTED;
     const bool need_ws = !direct || parts > 1;
-    const WsLayout lay = ws_layout(a.S, a.Hq, pool->head_dim, parts);
+    const WsLayout lay = ws_layout(a.S * a.NQ, a.Hq, pool->head_dim, parts);
     if (need_ws && (!workspace || !aligned16(workspace) || workspace_bytes < lay.bytes))
         return PKV_ERR_WORKSPACE;
     if (a.S == 0) return PKV_OK;
@@ -145,6 +153,9 @@ pkv_status run_decode(const DecodeArgs& a, void* out, int32_t out_dtype, int dir
     p.out = out;
     p.out_dtype = out_dtype;
     p.direct_single = direct;
+    const int G = a.Hq / pool->num_kv_heads;
+    p.num_queries = a.NQ;
+    p.queries_per_cta = 8 / G < a.NQ ? 8 / G : a.NQ;
     if (need_ws) {
         char* ws = static_cast<char*>(workspace);
         p.ws_m = reinterpret_cast<float*>(ws);
@@ -157,9 +168,17 @@ pkv_status run_decode(const DecodeArgs& a, void* out, int32_t out_dtype, int dir
         p.slot_out = append->slot_out;
     }
     p.err = err;
-    const int G = a.Hq / pool->num_kv_heads;
-    if (launch_decode_typed(p, pool->dtype, pool->head_dim, G, stream) != cudaSuccess)
+    if (a.NQ > 1) {
+        // several query rows per sequence: the tensor-core kernel only
+        const cudaError_t e =
+            pool->dtype == PKV_F16
+                ? pkv::launch_decode_mma<__half>(p, pool->head_dim, G, stream)
+                : pkv::launch_decode_mma<__nv_bfloat16>(p, pool->head_dim, G, stream);
+        if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
+        if (e != cudaSuccess) return PKV_ERR_CUDA;
+    } else if (launch_decode_typed(p, pool->dtype, pool->head_dim, G, stream) != cudaSuccess) {
         return PKV_ERR_CUDA;
+    }
     if (direct && parts > 1) {
         pkv::MergeParams mp{};
         mp.ws_m = p.ws_m;
@@ -172,6 +191,7 @@ pkv_status run_decode(const DecodeArgs& a, void* out, int32_t out_dtype, int dir
         mp.max_parts = parts;
         mp.partition_size = P;
         mp.skip_single = 1;
+        mp.num_queries = a.NQ;
         mp.out = out;
         mp.out_dtype = out_dtype;
         mp.err = err;
@@ -181,6 +201,11 @@ pkv_status run_decode(const DecodeArgs& a, void* out, int32_t out_dtype, int dir
 }
 
 }  // namespace
+
+bool pkv::use_tensor_cores(int group) {
+    const int e = g_engine.load(std::memory_order_relaxed);
+    return e == PKV_ENGINE_TENSOR_CORES || (e == PKV_ENGINE_AUTO && group >= 4);
+}
 
 // Partition scratch of pkv_paged_attention_decode_static_workspace, for callers
 // that cannot allocate device memory: one fixed array per device, held for the
@@ -214,6 +239,16 @@ pkv_status static_workspace(void** out) {
 extern "C" {
 
 int32_t pkv_version(void) { return 100; }
+
+pkv_status pkv_set_decode_engine(int32_t engine) {
+    if (engine != PKV_ENGINE_AUTO && engine != PKV_ENGINE_CUDA_CORES &&
+        engine != PKV_ENGINE_TENSOR_CORES)
+        return PKV_ERR_INVALID;
+    g_engine.store(engine, std::memory_order_relaxed);
+    return PKV_OK;
+}
+
+int32_t pkv_get_decode_engine(void) { return g_engine.load(std::memory_order_relaxed); }
 
 const char* pkv_status_str(pkv_status status) {
     switch (status) {
@@ -347,6 +382,28 @@ pkv_status pkv_paged_attention_decode_append(
                       static_cast<cudaStream_t>(stream), &app);
 }
 
+pkv_status pkv_paged_attention_decode_multi(
+    const pkv_pool* pool, const void* q, int32_t num_queries, int32_t num_seqs,
+    int32_t num_q_heads, const int32_t* block_tables, int32_t max_blocks_per_seq,
+    const int32_t* context_lens, int32_t max_context_len, float scale, void* out,
+    int32_t out_dtype, int32_t partition_size, void* workspace, size_t workspace_bytes,
+    void* stream) {
+    DecodeArgs a{pool, q, num_seqs, num_q_heads, block_tables, max_blocks_per_seq,
+                 context_lens, max_context_len, scale, partition_size};
+    pkv_status st = check_decode(a);
+    if (st != PKV_OK) return st;
+    if (num_queries < 1 || (int64_t)num_seqs * num_queries > INT32_MAX) return PKV_ERR_INVALID;
+    if (num_seqs > 0 && !out) return PKV_ERR_INVALID;
+    if (out_dtype != PKV_F32 && out_dtype != pool->dtype) return PKV_ERR_UNSUPPORTED;
+    if (pool->dtype == PKV_F32) return PKV_ERR_UNSUPPORTED;
+    a.NQ = num_queries;
+    const int32_t G = num_q_heads / pool->num_kv_heads;
+    if ((int64_t)pool->num_kv_heads * ((num_queries + 8 / G - 1) / (8 / G)) > INT32_MAX)
+        return PKV_ERR_UNSUPPORTED;
+    return run_decode(a, out, out_dtype, 1, workspace, workspace_bytes,
+                      static_cast<cudaStream_t>(stream));
+}
+
 pkv_status pkv_paged_attention_partitions(const pkv_pool* pool, const void* q, int32_t num_seqs,
                                           int32_t num_q_heads, const int32_t* block_tables,
                                           int32_t max_blocks_per_seq,
@@ -391,6 +448,7 @@ pkv_status pkv_lse_merge(const void* workspace, size_t workspace_bytes, int32_t 
     mp.max_parts = parts;
     mp.partition_size = partition_size;
     mp.skip_single = 0;
+    mp.num_queries = 1;
     mp.out = out;
     mp.out_dtype = out_dtype;
     mp.err = err;

@@ -1,11 +1,24 @@
-// decode_bf16.cu -- instantiates the paged decode kernels for __nv_bfloat16 pools.
+// decode_bf16.cu -- instantiates the paged decode kernels for __nv_bfloat16 pools: the
+// CUDA-core kernel (decode.cuh) and the tensor-core kernel for grouped-query
+// heads (decode_mma.cuh), chosen by the engine setting.
 #include "decode.cuh"
+#include "decode_mma.cuh"
 
 namespace pkv {
 
 template <>
 cudaError_t launch_decode<__nv_bfloat16>(const DecodeParams& p, int head_dim, int group, cudaStream_t stream) {
+    if (use_tensor_cores(group)) {
+        const cudaError_t e = launch_decode_mma_impl<__nv_bfloat16>(p, head_dim, group, stream);
+        if (e != cudaErrorNotSupported) return e;   // else: pool too large for a tensor map
+    }
     return launch_decode_impl<__nv_bfloat16>(p, head_dim, group, stream);
+}
+
+template <>
+cudaError_t launch_decode_mma<__nv_bfloat16>(const DecodeParams& p, int head_dim, int group,
+                                  cudaStream_t stream) {
+    return launch_decode_mma_impl<__nv_bfloat16>(p, head_dim, group, stream);
 }
 
 }  // namespace pkv

@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(const MergeParams p) {
     __shared__ float red[NWM][D + 1];
     __shared__ float smax[NWM];
     const int row = blockIdx.x;
-    const int s = row / p.num_q_heads;
+    const int s = row / (p.num_q_heads * p.num_queries);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int ctx = p.context_lens[s];
     const long long cap = (long long)p.max_parts * p.partition_size;
@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(const MergeParams p) {
 }
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
-    const unsigned rows = (unsigned)((long long)p.num_seqs * p.num_q_heads);
+    const unsigned rows = (unsigned)((long long)p.num_seqs * p.num_queries * p.num_q_heads);
     if (rows == 0) return cudaSuccess;
     if (p.head_dim == 64)
         lse_merge_kernel<64><<<rows, 128, 0, stream>>>(p);

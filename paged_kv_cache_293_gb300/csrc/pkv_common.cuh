@@ -39,6 +39,8 @@ struct DecodeParams {
     void* out;
     int32_t out_dtype;
     int32_t direct_single;  // 1: sequences with one partition write out directly
+    int32_t num_queries;    // query rows per sequence (1 for decode)
+    int32_t queries_per_cta;  // tensor-core kernel: queries sharing one CTA's 8 columns
     float* ws_m;
     float* ws_l;
     float* ws_o;
@@ -62,6 +64,7 @@ struct MergeParams {
     int32_t max_parts;
     int32_t partition_size;
     int32_t skip_single;    // 1: rows with <= 1 partition were written by the decode kernel
+    int32_t num_queries;    // rows are [num_seqs][num_queries][num_q_heads]
     void* out;
     int32_t out_dtype;
     unsigned int* err;
@@ -199,8 +202,16 @@ __device__ __forceinline__ void store_out(void* out, int32_t out_dtype, size_t i
 
 // ------------------------------------------------------------------ host launchers (internal)
 
+// Which decode kernel serves a group of G q heads per kv head on 16-bit pools
+// (set by pkv_set_decode_engine): tensor cores when G >= 4 by default.
+bool use_tensor_cores(int group);
+
 template <typename T>
 cudaError_t launch_decode(const DecodeParams& p, int head_dim, int group, cudaStream_t stream);
+// the tensor-core kernel alone (16-bit pools); cudaErrorNotSupported when the pool
+// cannot be described by a tensor map
+template <typename T>
+cudaError_t launch_decode_mma(const DecodeParams& p, int head_dim, int group, cudaStream_t stream);
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
 cudaError_t launch_slot_mapping(const int32_t* block_tables, int32_t max_blocks_per_seq,

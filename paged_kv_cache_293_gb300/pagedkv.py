@@ -50,6 +50,8 @@ _SIGS = {
                                                            _i32, _f32, _P, _i32, _i32, _P]),
     "pkv_paged_attention_decode_append": (_i32, [_PP, _P, _P, _P, _i32, _i32, _P, _i32, _P, _i32,
                                                  _f32, _P, _i32, _i32, _P, _sz, _P, _P]),
+    "pkv_paged_attention_decode_multi": (_i32, [_PP, _P, _i32, _i32, _i32, _P, _i32, _P, _i32,
+                                                _f32, _P, _i32, _i32, _P, _sz, _P]),
     "pkv_paged_attention_partitions": (_i32, [_PP, _P, _i32, _i32, _P, _i32, _P, _i32, _f32, _i32,
                                               _P, _sz, _P]),
     "pkv_lse_merge": (_i32, [_P, _sz, _i32, _i32, _i32, _P, _i32, _i32, _P, _i32, _P]),
@@ -58,6 +60,8 @@ _SIGS = {
     "pkv_get_device_error": (_i32, [ctypes.POINTER(ctypes.c_uint32), _P]),
     "pkv_status_str": (ctypes.c_char_p, [_i32]),
     "pkv_version": (_i32, []),
+    "pkv_set_decode_engine": (_i32, [_i32]),
+    "pkv_get_decode_engine": (_i32, []),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -121,6 +125,17 @@ def pkv_version():
     return lib.pkv_version()
 
 
+ENGINE_AUTO, ENGINE_CUDA_CORES, ENGINE_TENSOR_CORES = 0, 1, 2
+
+
+def pkv_set_decode_engine(engine):
+    _check(lib.pkv_set_decode_engine(int(engine)), "pkv_set_decode_engine")
+
+
+def pkv_get_decode_engine():
+    return lib.pkv_get_decode_engine()
+
+
 def pkv_slot_mapping(block_tables, positions, block_size, slot_mapping, token_seq=None,
                      stream=None):
     _contig(block_tables, positions, slot_mapping, token_seq)
@@ -182,6 +197,21 @@ def pkv_paged_attention_decode_append(q, k_pool, v_pool, k_new, v_new, block_tab
         block_tables.shape[1], _ptr(context_lens), int(max_context_len), float(scale), _ptr(out),
         _DTYPE[out.dtype], int(partition_size), _ptr(workspace), ws_bytes, _ptr(slot_mapping),
         _stream(stream, q)), "pkv_paged_attention_decode_append")
+
+
+def pkv_paged_attention_decode_multi(q, k_pool, v_pool, block_tables, context_lens, scale, out,
+                                     max_context_len, partition_size=0, workspace=None,
+                                     stream=None):
+    """q, out: [num_seqs][num_queries][num_q_heads][head_dim]."""
+    _contig(q, block_tables, context_lens, out, workspace)
+    pool = make_pool(k_pool, v_pool)
+    S, NQ, Hq, _ = q.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.pkv_paged_attention_decode_multi(
+        ctypes.byref(pool), _ptr(q), NQ, S, Hq, _ptr(block_tables), block_tables.shape[1],
+        _ptr(context_lens), int(max_context_len), float(scale), _ptr(out), _DTYPE[out.dtype],
+        int(partition_size), _ptr(workspace), ws_bytes, _stream(stream, q)),
+        "pkv_paged_attention_decode_multi")
 
 
 def pkv_paged_attention_decode_static_workspace(q, k_pool, v_pool, block_tables, context_lens,

@@ -24,6 +24,18 @@ def P():
     return pkv()
 
 
+@pytest.fixture
+def engine(P, request):
+    """Run the test with the decode engine given by the parameter, then restore auto."""
+    P.pkv_set_decode_engine(request.param)
+    yield request.param
+    P.pkv_set_decode_engine(P.ENGINE_AUTO)
+
+
+ENGINES = [0, 1, 2]          # auto, CUDA cores, tensor cores
+ENGINE_IDS = ["auto", "cuda_cores", "tensor_cores"]
+
+
 def run_decode(P, w, partition_size=None, out_dtype=torch.float32, block_tables=None,
                context_lens=None, max_context_len=None):
     bt = dev_i32(w.block_tables if block_tables is None else block_tables)
@@ -66,9 +78,12 @@ SMALL = [
 
 @pytest.mark.parametrize("dtype,Hq,Hkv,D,B,ctx", SMALL)
 @pytest.mark.parametrize("psize", [0, 64, 512, 4096])
-def test_decode_matches_oracle_small(P, dtype, Hq, Hkv, D, B, ctx, psize):
+@pytest.mark.parametrize("engine", ENGINES, ids=ENGINE_IDS, indirect=True)
+def test_decode_matches_oracle_small(P, engine, dtype, Hq, Hkv, D, B, ctx, psize):
     if psize and psize % B:
         pytest.skip("partition must be a multiple of the block size")
+    if dtype == "f32" and engine == 2:
+        pytest.skip("fp32 pools always use the CUDA-core kernel")
     w = workloads.build("small", dtype=dtype, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
                         block_size=B, context_lens=ctx, seed=len(ctx) + D, device=DEV)
     got = run_decode(P, w, partition_size=psize)
@@ -77,7 +92,8 @@ def test_decode_matches_oracle_small(P, dtype, Hq, Hkv, D, B, ctx, psize):
     assert_no_device_error(P)
 
 
-def test_split_equals_single_pass(P):
+@pytest.mark.parametrize("engine", [1, 2], ids=["cuda_cores", "tensor_cores"], indirect=True)
+def test_split_equals_single_pass(P, engine):
     w = workloads.build("split", dtype="f16", num_q_heads=16, num_kv_heads=4, head_dim=128,
                         block_size=16, context_lens=[4000, 700, 1, 2048, 513], seed=3, device=DEV)
     single = run_decode(P, w, partition_size=4096)
@@ -88,7 +104,8 @@ def test_split_equals_single_pass(P):
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-def test_16bit_output_is_oracle_rounded_within_one_ulp(P, dtype):
+@pytest.mark.parametrize("engine", [1, 2], ids=["cuda_cores", "tensor_cores"], indirect=True)
+def test_16bit_output_is_oracle_rounded_within_one_ulp(P, engine, dtype):
     w = workloads.build("out16", dtype=dtype, num_q_heads=8, num_kv_heads=2, head_dim=128,
                         block_size=16, context_lens=[7, 300, 1500], seed=5, device=DEV)
     tdt = workloads.TORCH_DTYPE[dtype]
@@ -103,7 +120,23 @@ def test_16bit_output_is_oracle_rounded_within_one_ulp(P, dtype):
     assert excess <= 0, "worst excess over one ulp: %g" % excess
 
 
-def test_block_permutation_gives_bit_identical_output(P):
+@pytest.mark.parametrize("engine", [1, 2], ids=["cuda_cores", "tensor_cores"], indirect=True)
+def test_engines_agree_and_hold_nan_rows_past_the_context(P, engine):
+    """Rows past a sequence's end in its last block may hold anything (here NaN and
+    inf); neither kernel lets them into the result."""
+    w = workloads.build("nanrows", dtype="bf16", num_q_heads=32, num_kv_heads=8, head_dim=128,
+                        block_size=32, context_lens=[5, 47, 1000, 70], seed=19, device=DEV)
+    for s, c in enumerate(w.context_lens):
+        last = w.block_tables[s, (c - 1) // 32]
+        w.k_pool[last, :, c % 32:] = float("nan") if c % 32 else w.k_pool[last, :, c % 32:]
+        w.v_pool[last, :, c % 32:] = float("inf") if c % 32 else w.v_pool[last, :, c % 32:]
+    got = run_decode(P, w, partition_size=0)
+    assert torch.isfinite(got).all()
+    assert max_abs(got, oracle_decode(w)) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("engine", [1, 2], ids=["cuda_cores", "tensor_cores"], indirect=True)
+def test_block_permutation_gives_bit_identical_output(P, engine):
     w = workloads.build("perm", dtype="bf16", num_q_heads=32, num_kv_heads=8, head_dim=128,
                         block_size=16, context_lens=[40, 900, 1234, 17], seed=8, device=DEV)
     base = run_decode(P, w, partition_size=512)
@@ -118,7 +151,8 @@ def test_block_permutation_gives_bit_identical_output(P):
     assert torch.equal(base, moved)
 
 
-def test_partitions_and_merge_match_oracle(P):
+@pytest.mark.parametrize("engine", [1, 2], ids=["cuda_cores", "tensor_cores"], indirect=True)
+def test_partitions_and_merge_match_oracle(P, engine):
     w = workloads.build("parts", dtype="f16", num_q_heads=8, num_kv_heads=4, head_dim=64,
                         block_size=16, context_lens=[0, 5, 512, 1025, 2000], seed=9, device=DEV)
     Pz, mcl = 256, int(w.context_lens.max())
@@ -278,6 +312,7 @@ def full_step(P, w):
 
 @pytest.mark.parametrize("name", ["tiny", "llama7b", "llama13b_b16", "llama13b_b32", "gqa_prefix"])
 def test_full_config_step_matches_oracle(P, name):
+    assert P.pkv_get_decode_engine() == P.ENGINE_AUTO
     w = workloads.make(name, seed=0, device=DEV)
     k0, v0 = host(w.k_pool).copy(), host(w.v_pool).copy()
     slots, out = full_step(P, w)
@@ -317,7 +352,9 @@ def test_long_context_split_matches_oracle_on_sampled_sequences(P):
     ("f32", 4, 4, 64, 16, [1, 17, 50, 100], 0),
     ("f16", 16, 2, 64, 16, [700, 31, 4096], 256),
 ])
-def test_fused_append_decode_equals_write_then_decode(P, dtype, Hq, Hkv, D, B, ctx, psize):
+@pytest.mark.parametrize("engine", ENGINES, ids=ENGINE_IDS, indirect=True)
+def test_fused_append_decode_equals_write_then_decode(P, engine, dtype, Hq, Hkv, D, B, ctx,
+                                                      psize):
     w = workloads.build("fused", dtype=dtype, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
                         block_size=B, context_lens=ctx, seed=31, device=DEV)
     k0, v0 = w.k_pool.clone(), w.v_pool.clone()
@@ -381,3 +418,38 @@ def test_swap_blocks_to_pinned_host_and_back(P):
     with pytest.raises(P.PagedKVError):                        # pageable host memory is refused
         P.pkv_swap_blocks(w.k_pool, w.v_pool, torch.zeros_like(hk), torch.zeros_like(hv),
                           dev_i32(out_pairs))
+
+
+# ------------------------------------------------------------------ several query rows per sequence
+
+@pytest.mark.parametrize("dtype,Hq,Hkv,D,B,ctx,nq,psize", [
+    ("f16", 8, 8, 128, 16, [40, 300, 17, 1500], 4, 0),      # MHA: all 4 queries in one pass
+    ("bf16", 32, 8, 128, 16, [5, 700, 64, 2000], 3, 512),   # G=4: 2 queries per pass, 2 passes
+    ("bf16", 16, 2, 64, 32, [33, 1025, 3], 2, 256),         # G=8: 1 query per pass; a row sees nothing
+    ("f16", 16, 8, 128, 16, [1, 9, 4096], 8, 1024),         # G=2, 8 queries -> 2 passes
+])
+def test_multi_query_decode_matches_oracle(P, dtype, Hq, Hkv, D, B, ctx, nq, psize):
+    w = workloads.build("multi", dtype=dtype, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                        block_size=B, context_lens=ctx, seed=41, device=DEV)
+    g = torch.Generator(device=DEV).manual_seed(5)
+    tdt = workloads.TORCH_DTYPE[dtype]
+    q = torch.randn((w.num_seqs, nq, Hq, D), generator=g, device=DEV).to(tdt)
+    mcl = w.max_context_len
+    ws_bytes = P.pkv_decode_workspace_bytes(w.k_pool, w.num_seqs * nq, Hq, mcl, psize)
+    ws = P.workspace_tensor(ws_bytes, DEV) if ws_bytes else None
+    out = torch.full((w.num_seqs, nq, Hq, D), float("nan"), dtype=torch.float32, device=DEV)
+    P.pkv_paged_attention_decode_multi(q, w.k_pool, w.v_pool, dev_i32(w.block_tables),
+                                       dev_i32(w.context_lens), w.scale, out, mcl, psize, ws)
+    torch.cuda.synchronize()
+    ref = oracle.paged_decode_multi(dtype, host(w.k_pool), host(w.v_pool), host(q),
+                                    w.block_tables, w.context_lens, w.scale)
+    assert max_abs(out, ref) <= TOL[dtype]
+    # the last query of each sequence sees the whole context: plain decode
+    P.pkv_set_decode_engine(P.ENGINE_TENSOR_CORES)
+    try:
+        w.q = q[:, -1].contiguous()
+        last = run_decode(P, w, partition_size=psize)
+    finally:
+        P.pkv_set_decode_engine(P.ENGINE_AUTO)
+    assert max_abs(out[:, -1], last.double().cpu().numpy()) <= 1e-5
+    assert_no_device_error(P)

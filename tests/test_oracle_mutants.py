@@ -43,6 +43,8 @@ MUTANTS = [
     ("swap copies K into V",
      "memcpy((char*)dst_v + (int64_t)dst * block_bytes, (const char*)src_v",
      "memcpy((char*)dst_v + (int64_t)dst * block_bytes, (const char*)src_k"),
+    ("multi-query sees one position too many",
+     "int32_t c = ctx - nq + 1 + j;", "int32_t c = ctx - nq + 2 + j;"),
     ("q rows read head-major",
      "qd[d] = load_as_double(q, dtype, ((int64_t)s * Hq + h) * D + d);\n            if (ctx == 0)",
      "qd[d] = load_as_double(q, dtype, ((int64_t)h * num_seqs + s) * D + d);\n            if (ctx == 0)"),

@@ -425,3 +425,43 @@ def test_swap_out_and_back_in_restores_the_pool():
     oracle.copy_blocks(k, v, pairs)
     oracle.swap_blocks(k1.copy(), v1.copy(), k1, v1, pairs)
     assert np.array_equal(k, k1) and np.array_equal(v, v1)
+
+
+# ------------------------------------------------------------------ several new tokens per sequence
+
+@pytest.mark.parametrize("dtype,ctx,nq,Hq,Hkv,D,B", [
+    ("f16", [20, 64, 9], 4, 8, 2, 64, 16),
+    ("bf16", [33, 5], 3, 4, 4, 128, 32),
+    ("f32", [3, 40], 5, 2, 1, 64, 16),       # first sequence: two queries see nothing
+])
+def test_multi_query_equals_causal_sdpa(dtype, ctx, nq, Hq, Hkv, D, B):
+    """The tail queries against torch SDPA with an explicit causal mask over the dense rows."""
+    rng = np.random.default_rng(14)
+    c = random_case(rng, dtype, ctx, Hq, Hkv, D, B)
+    qs, qx = rand_storage(rng, (len(ctx), nq, Hq, D), dtype)
+    scale = float(np.float32(0.2))
+    got = oracle.paged_decode_multi(dtype, c["k_pool"], c["v_pool"], qs, c["tables"], c["ctx"], scale)
+    G = Hq // Hkv
+    for s, L in enumerate(ctx):
+        K = torch.from_numpy(c["kx"][s]).permute(1, 0, 2).repeat_interleave(G, dim=0)  # [Hq, L, D]
+        V = torch.from_numpy(c["vx"][s]).permute(1, 0, 2).repeat_interleave(G, dim=0)
+        q = torch.from_numpy(qx[s]).permute(1, 0, 2)                                  # [Hq, nq, D]
+        pos = torch.arange(L)[None, :]
+        lim = (L - nq + torch.arange(nq))[:, None]
+        mask = pos <= lim                                                          # [nq, L]
+        for j in range(nq):
+            if L - nq + 1 + j <= 0:
+                assert np.all(got[s, j] == 0)
+                continue
+            want = torch.nn.functional.scaled_dot_product_attention(
+                q[:, j:j + 1], K, V, attn_mask=mask[j:j + 1], scale=scale)[:, 0].numpy()
+            np.testing.assert_allclose(got[s, j], want, rtol=0, atol=1e-12)
+
+
+def test_multi_query_with_one_query_is_decode():
+    rng = np.random.default_rng(15)
+    c = random_case(rng, "f16", [17, 90], 8, 2, 128, 16)
+    one = oracle.paged_decode_multi("f16", c["k_pool"], c["v_pool"], c["q"][:, None], c["tables"],
+                                    c["ctx"], 0.1)
+    dec = oracle.paged_decode("f16", c["k_pool"], c["v_pool"], c["q"], c["tables"], c["ctx"], 0.1)
+    assert np.array_equal(one[:, 0], dec)
