@@ -300,6 +300,73 @@ pkv_status pkv_swap_blocks(const pkv_pool* src, const pkv_pool* dst, const int32
                            int32_t num_pairs, void* stream);
 
 /*
+ * Block bookkeeping on the device.  "vLLM in Production", section
+ * "PagedAttention - Virtual Memory for the KV Cache": a sequence grows one
+ * block at a time as tokens arrive; "What Is vLLM", section "How does
+ * PagedAttention work?": blocks are allocated on demand, and sequences sharing
+ * a prefix share physical blocks through reference counting and copy-on-write.
+ * The state is three caller-owned device arrays; every call below is one
+ * launch on `stream` covering a whole batch of sequences, so a step's
+ * allocation needs no round trip to the host.
+ *   free_ids    int32 [num_blocks]: free physical ids; entries [0, *free_count) are valid
+ *   free_count  int32 [1]
+ *   refcount    int32 [num_blocks]: how many table entries point at each block
+ * Which free id a request receives depends on the order the GPU serves
+ * requests in; counts, statuses and the sequences' contents do not.
+ */
+typedef struct pkv_block_allocator {
+    int32_t* free_ids;
+    int32_t* free_count;
+    int32_t* refcount;
+    int32_t num_blocks;
+} pkv_block_allocator;
+
+/* Every block free, every count zero. */
+pkv_status pkv_allocator_reset(const pkv_block_allocator* alloc, void* stream);
+
+/*
+ * Sequence s grows from old_lens[s] to new_lens[s] tokens (int32 [num_seqs]
+ * each, device).  When old_lens[s] is not a multiple of B, the partly filled
+ * last block receives tokens: if other references to it remain, it is first
+ * copied to a fresh block (K and V, all kv heads) that replaces it in the
+ * table, and the original loses one reference (copy-on-write; of several
+ * holders appending in one call, the last reference keeps the original).  Then
+ * each logical block ceil(old / B) .. ceil(new / B) - 1 gets a fresh block
+ * with one reference.  seq_status[s] (int32, device, output): 0 done,
+ * 1 out of free blocks (what was allocated for s stays; later table entries
+ * are left as they were; the caller preempts or frees), 2 lengths invalid or
+ * the table row too short (nothing done for s).  Table rows of different
+ * sequences must be distinct memory.
+ */
+pkv_status pkv_allocate_for_append(const pkv_block_allocator* alloc, const pkv_pool* pool,
+                                   int32_t* block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t* old_lens, const int32_t* new_lens,
+                                   int32_t num_seqs, int32_t* seq_status, void* stream);
+
+/*
+ * Share blocks: for each pair i (src_dst_seqs int32 [num_pairs][2], device),
+ * sequence dst's first ceil(lens[i] / B) table entries become those of src
+ * and each of those blocks gains one reference (prefix sharing, or beam
+ * candidates branching from one sequence).  dst rows must hold no references
+ * (empty or freed) and must not be a src in the same call.
+ */
+pkv_status pkv_fork_sequences(const pkv_block_allocator* alloc, int32_t block_size,
+                              int32_t* block_tables, int32_t max_blocks_per_seq,
+                              const int32_t* src_dst_seqs, const int32_t* lens,
+                              int32_t num_pairs, void* stream);
+
+/*
+ * Release sequences (finished, or preempted after their blocks were swapped
+ * out): each of the first ceil(lens[i] / B) blocks of sequence seqs[i] loses
+ * one reference, a block left with none goes back to the free stack, and the
+ * table entries become -1.  seqs must be distinct.
+ */
+pkv_status pkv_free_sequences(const pkv_block_allocator* alloc, int32_t block_size,
+                              int32_t* block_tables, int32_t max_blocks_per_seq,
+                              const int32_t* seqs, const int32_t* lens, int32_t num_seqs,
+                              void* stream);
+
+/*
  * Synchronises stream, then reads and clears the current device's error word
  * into *flags (host pointer).  Returns PKV_ERR_DEVICE when any bit was set.
  */

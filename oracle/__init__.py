@@ -13,6 +13,11 @@ pages it follows and the readings it takes where the pages are silent):
                         ("What Is vLLM", section "How does PagedAttention work?").
 - ``partition_decode``  the same over ranges of P tokens, giving (m, l, o) per range.
 - ``lse_merge``         the log-sum-exp combination of such partial results.
+- ``Allocator``         block bookkeeping: a free-id stack and reference counts;
+                        allocate for append (with copy-on-write of a shared
+                        partly filled last block), fork, free ("vLLM in
+                        Production", "PagedAttention - Virtual Memory for the KV
+                        Cache"; "What Is vLLM", "How does PagedAttention work?").
 - ``paged_decode_multi`` several new tokens per sequence, each attending causally
                         to the cache up to itself ("Serving models with vLLM":
                         chunked prefill, speculative decoding).
@@ -57,6 +62,11 @@ def lib():
         _lib.oracle_kv_cache_write.argtypes = [ctypes.c_int, P, P, i32, i32, i32, i32, P, P, P, i32]
         _lib.oracle_copy_blocks.argtypes = [P, P, i32, i64, P, i32]
         _lib.oracle_swap_blocks.argtypes = [P, P, i32, P, P, i32, i64, P, i32]
+        _lib.oracle_allocator_reset.argtypes = [P, P, P, i32]
+        _lib.oracle_allocate_for_append.argtypes = [P, P, P, i32, P, P, i64, i32, P, i32, P, P,
+                                                    i32, P]
+        _lib.oracle_fork_sequences.argtypes = [P, i32, i32, P, i32, P, P, i32]
+        _lib.oracle_free_sequences.argtypes = [P, P, P, i32, i32, P, i32, P, P, i32]
         _lib.oracle_paged_decode_multi.argtypes = [ctypes.c_int, P, P, i32, i32, i32, i32, P, i32,
                                                    i32, i32, P, i32, P, f32, P]
         _lib.oracle_convert_to_double.argtypes = [ctypes.c_int, P, i64, P]
@@ -64,7 +74,9 @@ def lib():
         _lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
         for name in ("oracle_paged_decode", "oracle_partition_decode", "oracle_lse_merge",
                      "oracle_slot_mapping", "oracle_kv_cache_write", "oracle_copy_blocks",
-                     "oracle_swap_blocks", "oracle_paged_decode_multi"):
+                     "oracle_swap_blocks", "oracle_paged_decode_multi",
+                     "oracle_allocate_for_append", "oracle_fork_sequences",
+                     "oracle_free_sequences"):
             getattr(_lib, name).restype = ctypes.c_int
     return _lib
 
@@ -227,3 +239,43 @@ def paged_decode_multi(dtype, k_pool, v_pool, q, block_tables, context_lens, sca
                                            S, nq, Hq, _ptr(bt), bt.shape[1], _ptr(ctx),
                                            float(np.float32(scale)), _ptr(out)))
     return out
+
+
+class Allocator:
+    """Host state of the block bookkeeping, updated one sequence after another."""
+
+    def __init__(self, num_blocks):
+        self.num_blocks = int(num_blocks)
+        self.free_ids = np.zeros(num_blocks, np.int32)
+        self.free_count = np.zeros(1, np.int32)
+        self.refcount = np.zeros(num_blocks, np.int32)
+        lib().oracle_allocator_reset(_ptr(self.free_ids), _ptr(self.free_count),
+                                     _ptr(self.refcount), self.num_blocks)
+
+    def allocate_for_append(self, k_pool, v_pool, block_size, block_tables, old_lens, new_lens):
+        """In place on block_tables (contiguous int32) and the pools; returns statuses."""
+        assert block_tables.dtype == np.int32 and block_tables.flags.c_contiguous
+        old = np.ascontiguousarray(old_lens, np.int32)
+        new = np.ascontiguousarray(new_lens, np.int32)
+        status = np.zeros(old.shape, np.int32)
+        block_bytes = k_pool.nbytes // k_pool.shape[0]
+        _check(lib().oracle_allocate_for_append(
+            _ptr(self.free_ids), _ptr(self.free_count), _ptr(self.refcount), self.num_blocks,
+            _ptr(k_pool), _ptr(v_pool), block_bytes, int(block_size), _ptr(block_tables),
+            block_tables.shape[1], _ptr(old), _ptr(new), old.size, _ptr(status)))
+        return status
+
+    def fork(self, block_size, block_tables, pairs, lens):
+        pr = np.ascontiguousarray(pairs, np.int32).reshape(-1, 2)
+        ln = np.ascontiguousarray(lens, np.int32)
+        _check(lib().oracle_fork_sequences(_ptr(self.refcount), self.num_blocks, int(block_size),
+                                           _ptr(block_tables), block_tables.shape[1], _ptr(pr),
+                                           _ptr(ln), pr.shape[0]))
+
+    def free(self, block_size, block_tables, seqs, lens):
+        sq = np.ascontiguousarray(seqs, np.int32)
+        ln = np.ascontiguousarray(lens, np.int32)
+        _check(lib().oracle_free_sequences(_ptr(self.free_ids), _ptr(self.free_count),
+                                           _ptr(self.refcount), self.num_blocks, int(block_size),
+                                           _ptr(block_tables), block_tables.shape[1], _ptr(sq),
+                                           _ptr(ln), sq.size))

@@ -490,3 +490,109 @@ int oracle_paged_decode_multi(int dtype, const void* k_pool, const void* v_pool,
     }
     return err;
 }
+
+/*
+ * Block bookkeeping, one sequence after another ("vLLM in Production",
+ * section "PagedAttention - Virtual Memory for the KV Cache": a sequence grows
+ * one block at a time as tokens arrive; "What Is vLLM", section "How does
+ * PagedAttention work?": blocks allocated on demand, shared blocks reference
+ * counted and copied on write).  State: a stack of free ids (free_ids[0 ..
+ * *free_count)) and a reference count per block.
+ */
+void oracle_allocator_reset(int32_t* free_ids, int32_t* free_count, int32_t* refcount,
+                            int32_t num_blocks) {
+    for (int32_t i = 0; i < num_blocks; ++i) {
+        free_ids[i] = num_blocks - 1 - i; /* the top of the stack is block 0 */
+        refcount[i] = 0;
+    }
+    *free_count = num_blocks;
+}
+
+static int32_t take_free(int32_t* free_ids, int32_t* free_count) {
+    if (*free_count <= 0) return -1;
+    *free_count -= 1;
+    return free_ids[*free_count];
+}
+
+/*
+ * Sequence s grows from old_lens[s] to new_lens[s] tokens.  If its last block
+ * is partly filled (old % B != 0) and referenced by others, the sequence gets
+ * a private copy of it first (copy-on-write); then every new logical block
+ * gets a free block.  status[s]: 0 done, 1 no free block left, 2 bad lengths.
+ */
+int oracle_allocate_for_append(int32_t* free_ids, int32_t* free_count, int32_t* refcount,
+                               int32_t num_blocks, void* k_pool, void* v_pool, int64_t block_bytes,
+                               int32_t B, int32_t* block_tables, int32_t M, const int32_t* old_lens,
+                               const int32_t* new_lens, int32_t num_seqs, int32_t* status) {
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        int32_t old_len = old_lens[s], new_len = new_lens[s];
+        int32_t* row = block_tables + (int64_t)s * M;
+        status[s] = 0;
+        if (old_len < 0 || new_len < old_len || (int64_t)new_len > (int64_t)M * B) {
+            status[s] = 2;
+            continue;
+        }
+        if (new_len == old_len) continue;
+        if (old_len % B != 0) {
+            int32_t j = (old_len - 1) / B;
+            int32_t b = row[j];
+            if (b < 0 || b >= num_blocks) { status[s] = 2; continue; }
+            if (refcount[b] > 1) {
+                int32_t nb = take_free(free_ids, free_count);
+                if (nb < 0) { status[s] = 1; continue; }
+                memcpy((char*)k_pool + (int64_t)nb * block_bytes,
+                       (const char*)k_pool + (int64_t)b * block_bytes, (size_t)block_bytes);
+                memcpy((char*)v_pool + (int64_t)nb * block_bytes,
+                       (const char*)v_pool + (int64_t)b * block_bytes, (size_t)block_bytes);
+                refcount[b] -= 1;
+                refcount[nb] = 1;
+                row[j] = nb;
+            }
+        }
+        for (int32_t j = (old_len + B - 1) / B; j < (new_len + B - 1) / B; ++j) {
+            int32_t nb = take_free(free_ids, free_count);
+            if (nb < 0) { status[s] = 1; break; }
+            refcount[nb] = 1;
+            row[j] = nb;
+        }
+    }
+    return ORC_OK;
+}
+
+/* Sequence dst takes the first ceil(lens[i] / B) blocks of src; each gains a reference. */
+int oracle_fork_sequences(int32_t* refcount, int32_t num_blocks, int32_t B, int32_t* block_tables,
+                          int32_t M, const int32_t* pairs, const int32_t* lens, int32_t n) {
+    int rc = ORC_OK;
+    for (int32_t i = 0; i < n; ++i) {
+        int32_t src = pairs[2 * i], dst = pairs[2 * i + 1];
+        int32_t nb = (lens[i] + B - 1) / B;
+        if (lens[i] < 0 || nb > M) { rc = ORC_ERR_ARG; continue; }
+        for (int32_t j = 0; j < nb; ++j) {
+            int32_t b = block_tables[(int64_t)src * M + j];
+            if (b < 0 || b >= num_blocks) { rc = ORC_ERR_BLOCK; continue; }
+            block_tables[(int64_t)dst * M + j] = b;
+            refcount[b] += 1;
+        }
+    }
+    return rc;
+}
+
+/* Each listed sequence drops its references; blocks left unreferenced become free. */
+int oracle_free_sequences(int32_t* free_ids, int32_t* free_count, int32_t* refcount,
+                          int32_t num_blocks, int32_t B, int32_t* block_tables, int32_t M,
+                          const int32_t* seqs, const int32_t* lens, int32_t n) {
+    int rc = ORC_OK;
+    for (int32_t i = 0; i < n; ++i) {
+        int32_t* row = block_tables + (int64_t)seqs[i] * M;
+        int32_t nb = (lens[i] + B - 1) / B;
+        if (lens[i] < 0 || nb > M) { rc = ORC_ERR_ARG; continue; }
+        for (int32_t j = 0; j < nb; ++j) {
+            int32_t b = row[j];
+            row[j] = -1;
+            if (b < 0 || b >= num_blocks) { rc = ORC_ERR_BLOCK; continue; }
+            refcount[b] -= 1;
+            if (refcount[b] == 0) free_ids[(*free_count)++] = b;
+        }
+    }
+    return rc;
+}

@@ -530,6 +530,80 @@ pkv_status pkv_swap_blocks(const pkv_pool* src, const pkv_pool* dst, const int32
                : PKV_ERR_CUDA;
 }
 
+static bool allocator_ok(const pkv_block_allocator* a) {
+    return a && a->free_ids && a->free_count && a->refcount && a->num_blocks > 0;
+}
+
+static pkv::AllocatorState allocator_state(const pkv_block_allocator* a) {
+    return pkv::AllocatorState{a->free_ids, a->free_count, a->refcount, a->num_blocks};
+}
+
+pkv_status pkv_allocator_reset(const pkv_block_allocator* alloc, void* stream) {
+    if (!allocator_ok(alloc)) return PKV_ERR_INVALID;
+    return pkv::launch_allocator_reset(allocator_state(alloc), static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? PKV_OK
+               : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_allocate_for_append(const pkv_block_allocator* alloc, const pkv_pool* pool,
+                                   int32_t* block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t* old_lens, const int32_t* new_lens,
+                                   int32_t num_seqs, int32_t* seq_status, void* stream) {
+    if (!allocator_ok(alloc)) return PKV_ERR_INVALID;
+    pkv_status st = check_pool(pool);
+    if (st != PKV_OK) return st;
+    if (alloc->num_blocks != pool->num_blocks || max_blocks_per_seq <= 0 || num_seqs < 0)
+        return PKV_ERR_INVALID;
+    if (num_seqs == 0) return PKV_OK;
+    if (!block_tables || !old_lens || !new_lens || !seq_status) return PKV_ERR_INVALID;
+    unsigned int* err = nullptr;
+    st = error_word(&err);
+    if (st != PKV_OK) return st;
+    return pkv::launch_allocate_for_append(allocator_state(alloc), *pool, block_tables,
+                                           max_blocks_per_seq, old_lens, new_lens, num_seqs,
+                                           seq_status, err, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? PKV_OK
+               : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_fork_sequences(const pkv_block_allocator* alloc, int32_t block_size,
+                              int32_t* block_tables, int32_t max_blocks_per_seq,
+                              const int32_t* src_dst_seqs, const int32_t* lens,
+                              int32_t num_pairs, void* stream) {
+    if (!allocator_ok(alloc) || block_size <= 0 || max_blocks_per_seq <= 0 || num_pairs < 0)
+        return PKV_ERR_INVALID;
+    if (num_pairs == 0) return PKV_OK;
+    if (!block_tables || !src_dst_seqs || !lens) return PKV_ERR_INVALID;
+    unsigned int* err = nullptr;
+    pkv_status st = error_word(&err);
+    if (st != PKV_OK) return st;
+    return pkv::launch_fork_sequences(allocator_state(alloc), block_size, block_tables,
+                                      max_blocks_per_seq, src_dst_seqs, lens, num_pairs, err,
+                                      static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PKV_OK
+               : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_free_sequences(const pkv_block_allocator* alloc, int32_t block_size,
+                              int32_t* block_tables, int32_t max_blocks_per_seq,
+                              const int32_t* seqs, const int32_t* lens, int32_t num_seqs,
+                              void* stream) {
+    if (!allocator_ok(alloc) || block_size <= 0 || max_blocks_per_seq <= 0 || num_seqs < 0)
+        return PKV_ERR_INVALID;
+    if (num_seqs == 0) return PKV_OK;
+    if (!block_tables || !seqs || !lens) return PKV_ERR_INVALID;
+    unsigned int* err = nullptr;
+    pkv_status st = error_word(&err);
+    if (st != PKV_OK) return st;
+    return pkv::launch_free_sequences(allocator_state(alloc), block_size, block_tables,
+                                      max_blocks_per_seq, seqs, lens, num_seqs, err,
+                                      static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PKV_OK
+               : PKV_ERR_CUDA;
+}
+
 pkv_status pkv_get_device_error(uint32_t* flags, void* stream) {
     if (!flags) return PKV_ERR_INVALID;
     unsigned int* err = nullptr;

@@ -70,6 +70,14 @@ struct MergeParams {
     unsigned int* err;
 };
 
+// Device-side block bookkeeping (allocator.cu): a stack of free ids and counts.
+struct AllocatorState {
+    int32_t* free_ids;
+    int32_t* free_count;
+    int32_t* refcount;
+    int32_t num_blocks;
+};
+
 // ------------------------------------------------------------------ PTX helpers
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -221,6 +229,18 @@ cudaError_t launch_slot_mapping(const int32_t* block_tables, int32_t max_blocks_
 cudaError_t launch_cache_write(const pkv_pool& pool, const void* k_new, const void* v_new,
                                const int64_t* slot_mapping, int32_t num_tokens, unsigned int* err,
                                cudaStream_t stream);
+cudaError_t launch_allocator_reset(const AllocatorState& a, cudaStream_t stream);
+cudaError_t launch_allocate_for_append(const AllocatorState& a, const pkv_pool& pool,
+                                       int32_t* block_tables, int32_t M, const int32_t* old_lens,
+                                       const int32_t* new_lens, int32_t num_seqs,
+                                       int32_t* seq_status, unsigned int* err,
+                                       cudaStream_t stream);
+cudaError_t launch_fork_sequences(const AllocatorState& a, int32_t B, int32_t* block_tables,
+                                  int32_t M, const int32_t* pairs, const int32_t* lens, int32_t n,
+                                  unsigned int* err, cudaStream_t stream);
+cudaError_t launch_free_sequences(const AllocatorState& a, int32_t B, int32_t* block_tables,
+                                  int32_t M, const int32_t* seqs, const int32_t* lens, int32_t n,
+                                  unsigned int* err, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const pkv_pool& src, const pkv_pool& dst, const int32_t* pairs,
                                int32_t num_pairs, unsigned int* err, cudaStream_t stream);
 

@@ -36,8 +36,14 @@ class pkv_pool(ctypes.Structure):
                 ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32)]
 
 
+class pkv_block_allocator(ctypes.Structure):
+    _fields_ = [("free_ids", ctypes.c_void_p), ("free_count", ctypes.c_void_p),
+                ("refcount", ctypes.c_void_p), ("num_blocks", ctypes.c_int32)]
+
+
 _P, _i32, _i64, _sz, _f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
 _PP = ctypes.POINTER(pkv_pool)
+_PA = ctypes.POINTER(pkv_block_allocator)
 _SIGS = {
     "pkv_slot_mapping": (_i32, [_P, _i32, _i32, _P, _P, _i32, _i32, _P, _P]),
     "pkv_kv_cache_write": (_i32, [_PP, _P, _P, _P, _i32, _P]),
@@ -58,6 +64,10 @@ _SIGS = {
     "pkv_copy_blocks": (_i32, [_PP, _P, _i32, _P]),
     "pkv_swap_blocks": (_i32, [_PP, _PP, _P, _i32, _P]),
     "pkv_get_device_error": (_i32, [ctypes.POINTER(ctypes.c_uint32), _P]),
+    "pkv_allocator_reset": (_i32, [_PA, _P]),
+    "pkv_allocate_for_append": (_i32, [_PA, _PP, _P, _i32, _P, _P, _i32, _P, _P]),
+    "pkv_fork_sequences": (_i32, [_PA, _i32, _P, _i32, _P, _P, _i32, _P]),
+    "pkv_free_sequences": (_i32, [_PA, _i32, _P, _i32, _P, _P, _i32, _P]),
     "pkv_status_str": (ctypes.c_char_p, [_i32]),
     "pkv_version": (_i32, []),
     "pkv_set_decode_engine": (_i32, [_i32]),
@@ -271,6 +281,53 @@ def pkv_swap_blocks(src_k, src_v, dst_k, dst_v, src_dst_pairs, stream=None):
     n = src_dst_pairs.numel() // 2
     _check(lib.pkv_swap_blocks(ctypes.byref(src), ctypes.byref(dst), _ptr(src_dst_pairs), n,
                                _stream(stream, ref)), "pkv_swap_blocks")
+
+
+class BlockAllocator:
+    """Device arrays of the block bookkeeping (free-id stack, count, reference counts)."""
+
+    def __init__(self, num_blocks, device):
+        self.free_ids = torch.empty(num_blocks, dtype=torch.int32, device=device)
+        self.free_count = torch.zeros(1, dtype=torch.int32, device=device)
+        self.refcount = torch.zeros(num_blocks, dtype=torch.int32, device=device)
+        self.num_blocks = int(num_blocks)
+
+    def struct(self):
+        return pkv_block_allocator(self.free_ids.data_ptr(), self.free_count.data_ptr(),
+                                   self.refcount.data_ptr(), self.num_blocks)
+
+
+def pkv_allocator_reset(alloc, stream=None):
+    a = alloc.struct()
+    _check(lib.pkv_allocator_reset(ctypes.byref(a), _stream(stream, alloc.refcount)),
+           "pkv_allocator_reset")
+
+
+def pkv_allocate_for_append(alloc, k_pool, v_pool, block_tables, old_lens, new_lens, seq_status,
+                            stream=None):
+    _contig(block_tables, old_lens, new_lens, seq_status)
+    a, pool = alloc.struct(), make_pool(k_pool, v_pool)
+    S, M = block_tables.shape
+    _check(lib.pkv_allocate_for_append(ctypes.byref(a), ctypes.byref(pool), _ptr(block_tables), M,
+                                       _ptr(old_lens), _ptr(new_lens), S, _ptr(seq_status),
+                                       _stream(stream, block_tables)), "pkv_allocate_for_append")
+
+
+def pkv_fork_sequences(alloc, block_size, block_tables, src_dst_seqs, lens, stream=None):
+    _contig(block_tables, src_dst_seqs, lens)
+    a = alloc.struct()
+    _check(lib.pkv_fork_sequences(ctypes.byref(a), int(block_size), _ptr(block_tables),
+                                  block_tables.shape[1], _ptr(src_dst_seqs), _ptr(lens),
+                                  src_dst_seqs.numel() // 2, _stream(stream, block_tables)),
+           "pkv_fork_sequences")
+
+
+def pkv_free_sequences(alloc, block_size, block_tables, seqs, lens, stream=None):
+    _contig(block_tables, seqs, lens)
+    a = alloc.struct()
+    _check(lib.pkv_free_sequences(ctypes.byref(a), int(block_size), _ptr(block_tables),
+                                  block_tables.shape[1], _ptr(seqs), _ptr(lens), seqs.numel(),
+                                  _stream(stream, block_tables)), "pkv_free_sequences")
 
 
 def pkv_get_device_error(stream=None, device=None):

@@ -46,3 +46,19 @@ def compact_for_oracle(w, seqs, block_tables=None):
 def max_abs(gpu, ref):
     g = gpu.detach().float().cpu().numpy().astype(np.float64)
     return float(np.max(np.abs(g - ref))) if g.size else 0.0
+
+
+def check_allocator_invariants(free_ids, free_count, refcount, tables, lens, block_size):
+    """Counts equal the table references of the live positions; the free stack holds exactly
+    the unreferenced blocks, each once."""
+    N = refcount.size
+    refs = np.zeros(N, np.int64)
+    for s, L in enumerate(lens):
+        nb = -(-int(L) // block_size)
+        row = tables[s, :nb]
+        assert np.all((row >= 0) & (row < N)), "sequence %d has a bad table entry" % s
+        np.add.at(refs, row, 1)
+    assert np.array_equal(refs, refcount.astype(np.int64))
+    n = int(free_count)
+    free = np.sort(free_ids[:n])
+    assert np.array_equal(free, np.flatnonzero(refs == 0)), "free stack != unreferenced blocks"

@@ -45,6 +45,11 @@ MUTANTS = [
      "memcpy((char*)dst_v + (int64_t)dst * block_bytes, (const char*)src_k"),
     ("multi-query sees one position too many",
      "int32_t c = ctx - nq + 1 + j;", "int32_t c = ctx - nq + 2 + j;"),
+    ("copy-on-write skipped for shared blocks",
+     "            if (refcount[b] > 1) {\n                int32_t nb = take_free",
+     "            if (refcount[b] > 99) {\n                int32_t nb = take_free"),
+    ("freed blocks never return to the stack",
+     "if (refcount[b] == 0) free_ids[(*free_count)++] = b;", "(void)0;"),
     ("q rows read head-major",
      "qd[d] = load_as_double(q, dtype, ((int64_t)s * Hq + h) * D + d);\n            if (ctx == 0)",
      "qd[d] = load_as_double(q, dtype, ((int64_t)h * num_seqs + s) * D + d);\n            if (ctx == 0)"),

@@ -465,3 +465,86 @@ def test_multi_query_with_one_query_is_decode():
                                     c["ctx"], 0.1)
     dec = oracle.paged_decode("f16", c["k_pool"], c["v_pool"], c["q"], c["tables"], c["ctx"], 0.1)
     assert np.array_equal(one[:, 0], dec)
+
+
+# ------------------------------------------------------------------ block bookkeeping
+
+def test_toy_simulation_blocks_allocated_token_by_token():
+    """Growing the toy's eight requests (100 prompt tokens + their outputs) one token at a
+    time allocates blocks holding exactly the 960 slots the page prints, ceil(len/16) each."""
+    from gpu_helpers import check_allocator_invariants
+    g = golden("toy_kv_slots.json")
+    B = g["block_size"]
+    lens = np.array([g["prompt_tokens"] + n for n in g["output_lengths"]], np.int32)
+    N = 100
+    alloc = oracle.Allocator(N)
+    k = np.zeros((N, 1, B, 8), np.float32)
+    tables = np.full((len(lens), 16), -1, np.int32)
+    cur = np.zeros(len(lens), np.int32)
+    while np.any(cur < lens):
+        nxt = np.minimum(cur + 1, lens).astype(np.int32)
+        st = alloc.allocate_for_append(k, k, B, tables, cur, nxt)
+        assert np.all(st == 0)
+        cur = nxt
+    assert (N - int(alloc.free_count[0])) * B == g["paged_slots"]
+    for s, L in enumerate(lens):
+        assert np.sum(tables[s] >= 0) == -(-L // B)
+    check_allocator_invariants(alloc.free_ids, alloc.free_count[0], alloc.refcount, tables, lens, B)
+    alloc.free(B, tables, np.arange(len(lens)), lens)
+    assert int(alloc.free_count[0]) == N and np.all(alloc.refcount == 0)
+
+
+def test_hundred_tokens_take_four_blocks_of_32():
+    g = golden("hundred_tokens_four_blocks.json")
+    alloc = oracle.Allocator(10)
+    k = np.zeros((10, 1, g["block_size"], 8), np.float32)
+    tables = np.full((1, 8), -1, np.int32)
+    alloc.allocate_for_append(k, k, g["block_size"], tables, [0], [g["tokens"]])
+    assert 10 - int(alloc.free_count[0]) == g["blocks"]
+
+
+def test_fork_append_copy_on_write_free_keeps_every_sequence_intact():
+    """Prefix sharing by fork, then appends into the shared partly filled block: every holder
+    but the last reference gets a private copy, and each sequence still reads its own tokens."""
+    from gpu_helpers import check_allocator_invariants
+    B, N, M = 16, 64, 8
+    rng = np.random.default_rng(3)
+    alloc = oracle.Allocator(N)
+    k = rng.standard_normal((N, 2, B, 64)).astype(np.float32)
+    v = rng.standard_normal((N, 2, B, 64)).astype(np.float32)
+    tables = np.full((4, M), -1, np.int32)
+    lens = np.array([40, 0, 0, 0], np.int32)                 # sequence 0: 40 tokens, 3 blocks
+    assert np.all(alloc.allocate_for_append(k, v, B, tables, [0, 0, 0, 0], lens) == 0)
+    alloc.fork(B, tables, [[0, 1], [0, 2]], [40, 40])          # 1 and 2 share all of 0's blocks
+    lens = np.array([40, 40, 40, 0], np.int32)
+    check_allocator_invariants(alloc.free_ids, alloc.free_count[0], alloc.refcount, tables, lens, B)
+    q = rng.standard_normal((4, 2, 64)).astype(np.float32)
+    before = oracle.paged_decode("f32", k, v, q[:3], tables[:3], lens[:3], 0.125)
+    shared_last = tables[0, 2]
+    used_before = N - int(alloc.free_count[0])
+    new = np.array([41, 45, 40, 0], np.int32)                # 0 and 1 append, 2 does not
+    assert np.all(alloc.allocate_for_append(k, v, B, tables, lens, new) == 0)
+    # both appenders copy (sequence 2 still holds the original), nothing else is allocated
+    assert N - int(alloc.free_count[0]) == used_before + 2
+    assert tables[2, 2] == shared_last and tables[0, 2] != shared_last != tables[1, 2]
+    assert np.array_equal(k[tables[0, 2]], k[shared_last]) and np.array_equal(v[tables[1, 2]], v[shared_last])
+    after = oracle.paged_decode("f32", k, v, q[:3], tables[:3], lens[:3], 0.125)
+    assert np.array_equal(before, after)
+    check_allocator_invariants(alloc.free_ids, alloc.free_count[0], alloc.refcount, tables, new, B)
+    alloc.free(B, tables, [0, 1, 2], new[:3])
+    assert int(alloc.free_count[0]) == N and np.all(alloc.refcount == 0)
+
+
+def test_last_reference_keeps_its_block():
+    B, N = 16, 8
+    alloc = oracle.Allocator(N)
+    k = np.zeros((N, 1, B, 8), np.float32)
+    tables = np.full((2, 10), -1, np.int32)
+    alloc.allocate_for_append(k, k, B, tables, [0, 0], [20, 0])
+    alloc.fork(B, tables, [[0, 1]], [20])
+    alloc.free(B, tables, [1], [20])
+    owned = tables[0, 1]
+    assert np.all(alloc.allocate_for_append(k, k, B, tables, [20, 0], [21, 0]) == 0)
+    assert tables[0, 1] == owned                            # refcount 1: written in place
+    st = alloc.allocate_for_append(k, k, B, tables, [21, 0], [21 + 16 * 7, 0])
+    assert st[0] == 1                                        # only 6 free blocks were left
