@@ -53,8 +53,9 @@ def read_peaks():
         return 6800.0, "fallback"
 
 
-def read_traffic(kernel_file, workload):
-    """DRAM bytes per launch from the committed ncu summary, if it still matches the source."""
+def read_traffic(workload):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu record of this
+    workload, or None when there is none or the kernel source it names has changed since."""
     import hashlib
     summ = os.path.join(ROOT, "profiles", "decode_%s_traffic.txt" % workload)
     if not os.path.exists(summ):
@@ -66,7 +67,7 @@ def read_traffic(kernel_file, workload):
                 k, v = line.split(":", 1)
                 vals[k.strip()] = v.strip()
     h = hashlib.sha256()
-    for name in kernel_file:
+    for name in vals.get("source_files", "").split():
         with open(os.path.join(ROOT, "paged_kv_cache_293_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     if vals.get("source_sha256") != h.hexdigest():
@@ -300,7 +301,11 @@ def run_ours(args):
     peak, peak_kind = read_peaks()
     value = world * total / (step_ms_max * 1e-3) / 1e9
     dec_gbs = dec_unique / (dec_ms * 1e-3) / 1e9
-    traffic = read_traffic(["decode.cuh", "pkv_common.cuh"], args.workload)
+    traffic = read_traffic(args.workload)
+    tensor = (w.dtype != "f32" and w.num_q_heads // w.num_kv_heads >= 4
+              and P.pkv_get_decode_engine() == P.ENGINE_AUTO)
+    kernel_name = ("paged_decode_mma_kernel" if tensor else "paged_decode_kernel") + (
+        " + lse_merge_kernel" if st.split else "")
 
     if rank != 0:
         return
@@ -342,7 +347,7 @@ def run_ours(args):
             "seed": args.seed,
         },
         "roofline": {
-            "kernel": "paged_decode_kernel (+ lse_merge_kernel when partitioned)",
+            "kernel": kernel_name,
             "bound": "hbm", "achieved": round(dec_gbs, 2), "peak": peak, "unit": "GB/s",
             "frac": round(dec_gbs / peak, 4), "peak_kind": peak_kind,
             "traffic": traffic, "algorithmic_bytes": dec_unique,
