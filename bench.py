@@ -166,8 +166,8 @@ def max_over_ranks(x, world, device):
 class Step:
     """Device buffers and the launch sequence of one decode step through the binding."""
 
-    def __init__(self, P, w, device):
-        self.P, self.w, self.dev = P, w, device
+    def __init__(self, P, w, device, fused=True):
+        self.P, self.w, self.dev, self.fused = P, w, device, fused
         i32 = lambda a: torch.as_tensor(np.ascontiguousarray(a, np.int32), device=device)
         self.bt = i32(w.block_tables)
         self.pos = i32(w.positions)
@@ -183,19 +183,30 @@ class Step:
                                               self.psize)
         self.ws = P.workspace_tensor(nbytes, device) if nbytes else None
         self.split = nbytes > 0
-        self.launches = 3 + (1 if self.split else 0) + (1 if self.pairs is not None else 0)
+        self.launches = ((1 if fused else 3) + (1 if self.split else 0)
+                         + (1 if self.pairs is not None else 0))
 
     def pre_decode(self):
+        """Work before the decode call: the copy-on-write copy, and unless the append is
+        fused into the decode launch, slot mapping and the cache write."""
         P, w = self.P, self.w
         if self.pairs is not None:
             P.pkv_copy_blocks(w.k_pool, w.v_pool, self.pairs)
-        P.pkv_slot_mapping(self.bt, self.pos, w.block_size, self.slots)
-        P.pkv_kv_cache_write(w.k_pool, w.v_pool, w.k_new, w.v_new, self.slots)
+        if not self.fused:
+            P.pkv_slot_mapping(self.bt, self.pos, w.block_size, self.slots)
+            P.pkv_kv_cache_write(w.k_pool, w.v_pool, w.k_new, w.v_new, self.slots)
 
     def decode(self):
+        """The decode call; fused: it also computes each new token's slot and writes its
+        K/V rows (one launch instead of three, same result)."""
         P, w = self.P, self.w
-        P.pkv_paged_attention_decode(w.q, w.k_pool, w.v_pool, self.bt, self.ctx, w.scale,
-                                     self.out, self.mcl, self.psize, self.ws)
+        if self.fused:
+            P.pkv_paged_attention_decode_append(w.q, w.k_pool, w.v_pool, w.k_new, w.v_new, self.bt,
+                                                self.ctx, w.scale, self.out, self.mcl, self.psize,
+                                                self.ws, slot_mapping=self.slots)
+        else:
+            P.pkv_paged_attention_decode(w.q, w.k_pool, w.v_pool, self.bt, self.ctx, w.scale,
+                                         self.out, self.mcl, self.psize, self.ws)
 
 
 def step_bytes(w, psize):
@@ -258,7 +269,7 @@ def run_ours(args):
     from paged_kv_cache_293_gb300 import pagedkv as P
 
     w = workloads.make(args.workload, seed=args.seed + rank, device=device)
-    st = Step(P, w, device)
+    st = Step(P, w, device, fused=not args.unfused)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
 
@@ -297,6 +308,9 @@ def run_ours(args):
     e2e_ms_max = max_over_ranks(e2e["ms"], world, device)
 
     dec_logical, dec_unique, other = step_bytes(w, st.psize if st.split else 0)
+    if st.fused:  # the decode launch also reads the new rows and writes them into the pool
+        dec_unique += accounting.write_bytes(w.num_seqs, w.num_kv_heads, w.head_dim,
+                                             workloads.ELEM_BYTES[w.dtype])
     total = dec_logical + other
     peak, peak_kind = read_peaks()
     value = world * total / (step_ms_max * 1e-3) / 1e9
@@ -345,6 +359,8 @@ def run_ours(args):
             "l2": "flushed by a 256 MiB write before every timed step (outside the events)",
             "parallelism": "replicas, one batch per GPU" if world > 1 else "single GPU",
             "seed": args.seed,
+            "path": ("decode with the append fused (slot, write, attention in one launch)"
+                     if st.fused else "slot mapping, cache write, decode: three launches"),
         },
         "roofline": {
             "kernel": kernel_name,
@@ -461,6 +477,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.CONFIGS))
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--unfused", action="store_true",
+                    help="slot mapping, cache write and decode as three launches")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

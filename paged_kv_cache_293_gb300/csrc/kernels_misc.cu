@@ -136,6 +136,9 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(const MergeParams p) {
     constexpr int NWM = 4, DPL = D / 32;
     __shared__ float red[NWM][D + 1];
     __shared__ float smax[NWM];
+    // Launched as a programmatic dependent of the decode kernel: the launch overlaps
+    // the decode's last CTAs, and this waits for the decode grid's results here.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int row = blockIdx.x;
     const int s = row / (p.num_q_heads * p.num_queries);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -189,13 +192,19 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(const MergeParams p) {
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
     const unsigned rows = (unsigned)((long long)p.num_seqs * p.num_queries * p.num_q_heads);
     if (rows == 0) return cudaSuccess;
-    if (p.head_dim == 64)
-        lse_merge_kernel<64><<<rows, 128, 0, stream>>>(p);
-    else if (p.head_dim == 128)
-        lse_merge_kernel<128><<<rows, 128, 0, stream>>>(p);
-    else
-        return cudaErrorInvalidValue;
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(rows);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (p.head_dim == 64) return cudaLaunchKernelEx(&cfg, lse_merge_kernel<64>, p);
+    if (p.head_dim == 128) return cudaLaunchKernelEx(&cfg, lse_merge_kernel<128>, p);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace pkv

@@ -2,8 +2,7 @@
 
 Which free id a request gets depends on the order the GPU serves the atomics
 in, so ids are not compared.  What is unique is: statuses, how many blocks are
-taken, the counts of blocks that existed before the call, and every sequence's
-contents; the rest must be valid: counts equal table references and the free
+taken, the multiset of reference counts, and every sequence's contents; the rest must be valid: counts equal table references and the free
 stack holds exactly the unreferenced blocks.
 """
 import numpy as np
@@ -76,7 +75,6 @@ def test_prefill_fork_append_free_cycle(P):
     grow = np.where(live, rng.integers(1, 21, S), 0).astype(np.int32)
     grow[8] = 0
     new = (lens + grow).astype(np.int32)
-    old_refs = rc.copy()
     P.pkv_allocate_for_append(alloc, w.k_pool, w.v_pool, tables, dev_i32(lens), dev_i32(new),
                               status)
     st_ref = ref.allocate_for_append(kh, vh, B, ref_tables, lens, new)
@@ -84,8 +82,8 @@ def test_prefill_fork_append_free_cycle(P):
     assert np.array_equal(status.cpu().numpy(), st_ref) and np.all(st_ref == 0)
     fi, fc, rc = state(alloc)
     assert fc == int(ref.free_count[0])                     # same number of blocks taken
-    existed = old_refs > 0
-    assert np.array_equal(rc[existed], ref.refcount[existed])   # counts of older blocks agree
+    # the ids differ from the oracle's, the multiset of counts does not
+    assert np.array_equal(np.sort(rc), np.sort(ref.refcount))
     check_allocator_invariants(fi, fc, rc, tables.cpu().numpy(), new, B)
     after = oracle.paged_decode("bf16", host(w.k_pool), host(w.v_pool), host(q)[live],
                                 tables.cpu().numpy()[live], lens[live], 0.1)
