@@ -371,6 +371,7 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": {"value": round(world * total / (e2e_ms_max * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms_max, 5),
+                "overlap": "input and output copies on their own stream, two steps deep",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
         "gpu_launches": st.launches * args.steps,
         "clocks": clocks.summary(),
@@ -380,33 +381,69 @@ def run_ours(args):
 
 
 def run_e2e(P, w, st, args, device, flush):
-    """Same step, inputs copied from pinned host memory each step and the output read back."""
-    pin = lambda t: t.detach().cpu().pin_memory()
-    h_q, h_k, h_v = pin(w.q), pin(w.k_new), pin(w.v_new)
-    h_bt, h_pos, h_ctx = pin(st.bt), pin(st.pos), pin(st.ctx)
-    h_out = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
-    stream = torch.cuda.current_stream(device)
-    pairs = [(h_q, w.q), (h_k, w.k_new), (h_v, w.v_new), (h_bt, st.bt), (h_pos, st.pos),
-             (h_ctx, st.ctx)]
-    h2d = sum(h.numel() * h.element_size() for h, _ in pairs)
-    d2h = h_out.numel() * h_out.element_size()
-    n = max(3, args.steps // 4)
-    times = []
-    for i in range(n + args.warmup):
-        flush.zero_()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for h, d in pairs:
-            d.copy_(h, non_blocking=True)
-        st.pre_decode()
-        st.decode()
-        h_out.copy_(st.out, non_blocking=True)
-        e1.record(stream)
-        e1.synchronize()
-        if i >= args.warmup:
-            times.append(e0.elapsed_time(e1))
-    return {"ms": sum(times) / len(times), "h2d": h2d, "d2h": d2h}
+    """The same step end to end through the binding: every step copies its inputs (q, new
+    K/V rows, block tables, positions, lengths) from pinned host memory and reads its output
+    back.  As a serving loop would, the copies run on their own stream two steps deep: step
+    i+1's inputs go in while step i computes, and step i's output comes back while step i+1
+    computes.  The KV pool (larger than L2) stays resident.  Timed with CUDA events from the
+    first input copy to the last output copy."""
+    names = ["q", "k_new", "v_new", "bt", "pos", "ctx"]
+    dev_src = {"q": w.q, "k_new": w.k_new, "v_new": w.v_new, "bt": st.bt, "pos": st.pos,
+               "ctx": st.ctx}
+    host_in = {k: v.detach().cpu().pin_memory() for k, v in dev_src.items()}
+    bufs = [{k: torch.empty_like(v) for k, v in dev_src.items()} for _ in range(2)]
+    outs = [torch.empty_like(st.out) for _ in range(2)]
+    h_out = [torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory() for _ in range(2)]
+    h2d = sum(h.numel() * h.element_size() for h in host_in.values())
+    d2h = h_out[0].numel() * h_out[0].element_size()
+    comp = torch.cuda.current_stream(device)
+    copy = torch.cuda.Stream(device)
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    computed = [torch.cuda.Event() for _ in range(2)]
+    out_read = [torch.cuda.Event() for _ in range(2)]
+    saved = (w.q, w.k_new, w.v_new, st.bt, st.pos, st.ctx, st.out)
+
+    def load(i):
+        b = i % 2
+        if i >= 2:
+            copy.wait_event(computed[b])        # step i - 2 is done with this buffer
+        with torch.cuda.stream(copy):
+            for k in names:
+                bufs[b][k].copy_(host_in[k], non_blocking=True)
+        in_ready[b].record(copy)
+
+    def run(n):
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(device)
+        t0.record(copy)
+        load(0)
+        for i in range(n):
+            b = i % 2
+            if i + 1 < n:
+                load(i + 1)
+            comp.wait_event(in_ready[b])
+            if i >= 2:
+                comp.wait_event(out_read[b])    # step i - 2's output has been read back
+            w.q, w.k_new, w.v_new = bufs[b]["q"], bufs[b]["k_new"], bufs[b]["v_new"]
+            st.bt, st.pos, st.ctx, st.out = bufs[b]["bt"], bufs[b]["pos"], bufs[b]["ctx"], outs[b]
+            st.pre_decode()
+            st.decode()
+            computed[b].record(comp)
+            copy.wait_event(computed[b])
+            with torch.cuda.stream(copy):
+                h_out[b].copy_(outs[b], non_blocking=True)
+            out_read[b].record(copy)
+        t1.record(copy)
+        t1.synchronize()
+        return t0.elapsed_time(t1) / n
+
+    try:
+        run(max(3, args.warmup))
+        ms = run(max(3, args.steps // 4))
+    finally:
+        w.q, w.k_new, w.v_new, st.bt, st.pos, st.ctx, st.out = saved
+    return {"ms": ms, "h2d": h2d, "d2h": d2h}
 
 
 def run_reference(args):
