@@ -372,6 +372,7 @@ def run_ours(args):
         "e2e": {"value": round(world * total / (e2e_ms_max * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms_max, 5),
                 "overlap": "input and output copies on their own stream, two steps deep",
+                "l2": "consecutive steps alternate between two KV pools (two layers)",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
         "gpu_launches": st.launches * args.steps,
         "clocks": clocks.summary(),
@@ -385,8 +386,9 @@ def run_e2e(P, w, st, args, device, flush):
     K/V rows, block tables, positions, lengths) from pinned host memory and reads its output
     back.  As a serving loop would, the copies run on their own stream two steps deep: step
     i+1's inputs go in while step i computes, and step i's output comes back while step i+1
-    computes.  The KV pool (larger than L2) stays resident.  Timed with CUDA events from the
-    first input copy to the last output copy."""
+    computes.  Consecutive steps read two different KV pools of the batch's shape (two
+    layers' caches, each larger than L2), so no step finds the previous step's pages in L2.
+    Timed with CUDA events from the first input copy to the last output copy."""
     names = ["q", "k_new", "v_new", "bt", "pos", "ctx"]
     dev_src = {"q": w.q, "k_new": w.k_new, "v_new": w.v_new, "bt": st.bt, "pos": st.pos,
                "ctx": st.ctx}
@@ -401,7 +403,8 @@ def run_e2e(P, w, st, args, device, flush):
     in_ready = [torch.cuda.Event() for _ in range(2)]
     computed = [torch.cuda.Event() for _ in range(2)]
     out_read = [torch.cuda.Event() for _ in range(2)]
-    saved = (w.q, w.k_new, w.v_new, st.bt, st.pos, st.ctx, st.out)
+    pools = [(w.k_pool, w.v_pool), (w.k_pool.clone(), w.v_pool.clone())]
+    saved = (w.q, w.k_new, w.v_new, st.bt, st.pos, st.ctx, st.out, w.k_pool, w.v_pool)
 
     def load(i):
         b = i % 2
@@ -427,6 +430,7 @@ def run_e2e(P, w, st, args, device, flush):
                 comp.wait_event(out_read[b])    # step i - 2's output has been read back
             w.q, w.k_new, w.v_new = bufs[b]["q"], bufs[b]["k_new"], bufs[b]["v_new"]
             st.bt, st.pos, st.ctx, st.out = bufs[b]["bt"], bufs[b]["pos"], bufs[b]["ctx"], outs[b]
+            w.k_pool, w.v_pool = pools[b]
             st.pre_decode()
             st.decode()
             computed[b].record(comp)
@@ -442,7 +446,8 @@ def run_e2e(P, w, st, args, device, flush):
         run(max(3, args.warmup))
         ms = run(max(3, args.steps // 4))
     finally:
-        w.q, w.k_new, w.v_new, st.bt, st.pos, st.ctx, st.out = saved
+        w.q, w.k_new, w.v_new, st.bt, st.pos, st.ctx, st.out, w.k_pool, w.v_pool = saved
+        del pools
     return {"ms": ms, "h2d": h2d, "d2h": d2h}
 
 
