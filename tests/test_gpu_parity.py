@@ -453,3 +453,47 @@ def test_multi_query_decode_matches_oracle(P, dtype, Hq, Hkv, D, B, ctx, nq, psi
         P.pkv_set_decode_engine(P.ENGINE_AUTO)
     assert max_abs(out[:, -1], last.double().cpu().numpy()) <= 1e-5
     assert_no_device_error(P)
+
+
+# ------------------------------------------------------------------ exactly what bench.py times
+
+def _ulp_excess(got, ref, dtype):
+    tdt = workloads.TORCH_DTYPE[dtype]
+    ref_t = torch.from_numpy(ref)
+    ref_r = ref_t.to(tdt).double()
+    mant, floor = (10, 2.0 ** -24) if dtype == "f16" else (7, 2.0 ** -133)
+    ulp = (ref_r.abs().clamp_min(1e-38).log2().floor() - mant).exp2().clamp_min(floor)
+    return ((got.double().cpu() - ref_r).abs() - ulp).max().item()
+
+
+@pytest.mark.parametrize("name", ["llama13b_b16", "gqa_prefix", "long_splitk"])
+def test_bench_step_matches_oracle_at_full_size(P, name):
+    """bench.py's own Step (fused append + decode, output in the pool type, the partition
+    size and engine it uses) on the full batch: slots and pools bit-exact, output equal to
+    the oracle rounded to the output type within one unit in the last place (sampled
+    sequences for the long contexts)."""
+    import bench
+    w = workloads.make(name, seed=0, device=DEV)
+    st = bench.Step(P, w, torch.device(DEV), fused=True)
+    seqs = np.arange(w.num_seqs) if name != "long_splitk" else np.array([0, 5])
+    bt_before = w.block_tables
+    if name == "llama13b_b16":
+        k0, v0 = host(w.k_pool).copy(), host(w.v_pool).copy()
+    st.pre_decode()
+    st.decode()
+    torch.cuda.synchronize()
+    ref_slots = oracle.slot_mapping(bt_before, w.positions, w.block_size)
+    assert np.array_equal(st.slots.cpu().numpy(), ref_slots)
+    if name == "llama13b_b16":
+        oracle.kv_cache_write(w.dtype, k0, v0, host(w.k_new), host(w.v_new), ref_slots)
+        assert np.array_equal(host(w.k_pool), k0) and np.array_equal(host(w.v_pool), v0)
+    if name == "long_splitk":
+        k, v, bt, ctx, q = compact_for_oracle(w, seqs)
+        ref = oracle.paged_decode(w.dtype, k, v, q, bt, ctx, w.scale)
+    else:
+        ref = oracle.paged_decode(w.dtype, host(w.k_pool), host(w.v_pool), host(w.q),
+                                  w.block_tables, w.context_lens, w.scale)
+    got = st.out[torch.as_tensor(seqs, device=DEV)]
+    assert got.dtype == w.q.dtype
+    assert _ulp_excess(got, ref, w.dtype) <= 0
+    assert_no_device_error(P)
