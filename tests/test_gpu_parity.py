@@ -457,21 +457,23 @@ def test_multi_query_decode_matches_oracle(P, dtype, Hq, Hkv, D, B, ctx, nq, psi
 
 # ------------------------------------------------------------------ exactly what bench.py times
 
-def _ulp_excess(got, ref, dtype):
+def _ulp_excess(got, ref, dtype, ulps=1):
+    """How far the 16-bit output lies beyond `ulps` units in the last place of the oracle
+    rounded to that type (<= 0: within)."""
     tdt = workloads.TORCH_DTYPE[dtype]
     ref_t = torch.from_numpy(ref)
     ref_r = ref_t.to(tdt).double()
     mant, floor = (10, 2.0 ** -24) if dtype == "f16" else (7, 2.0 ** -133)
     ulp = (ref_r.abs().clamp_min(1e-38).log2().floor() - mant).exp2().clamp_min(floor)
-    return ((got.double().cpu() - ref_r).abs() - ulp).max().item()
+    return ((got.double().cpu() - ref_r).abs() - ulps * ulp).max().item()
 
 
 @pytest.mark.parametrize("name", ["llama13b_b16", "gqa_prefix", "long_splitk"])
 def test_bench_step_matches_oracle_at_full_size(P, name):
     """bench.py's own Step (fused append + decode, output in the pool type, the partition
-    size and engine it uses) on the full batch: slots and pools bit-exact, output equal to
-    the oracle rounded to the output type within one unit in the last place (sampled
-    sequences for the long contexts)."""
+    size and engine it uses) on the full batch: slots and pools bit-exact; the output within
+    the stated 2e-3 of the unrounded oracle, and within two units in the last place of the
+    oracle rounded to the output type (sampled sequences for the long contexts)."""
     import bench
     w = workloads.make(name, seed=0, device=DEV)
     st = bench.Step(P, w, torch.device(DEV), fused=True)
@@ -495,5 +497,6 @@ def test_bench_step_matches_oracle_at_full_size(P, name):
                                   w.block_tables, w.context_lens, w.scale)
     got = st.out[torch.as_tensor(seqs, device=DEV)]
     assert got.dtype == w.q.dtype
-    assert _ulp_excess(got, ref, w.dtype) <= 0
+    assert max_abs(got, ref) <= TOL[w.dtype]
+    assert _ulp_excess(got, ref, w.dtype, ulps=2) <= 0
     assert_no_device_error(P)
