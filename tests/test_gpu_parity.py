@@ -109,14 +109,10 @@ def test_16bit_output_is_oracle_rounded_within_one_ulp(P, engine, dtype):
     w = workloads.build("out16", dtype=dtype, num_q_heads=8, num_kv_heads=2, head_dim=128,
                         block_size=16, context_lens=[7, 300, 1500], seed=5, device=DEV)
     tdt = workloads.TORCH_DTYPE[dtype]
-    got = run_decode(P, w, out_dtype=tdt, partition_size=512).double().cpu()
-    ref = torch.from_numpy(oracle_decode(w))
-    ref_r = ref.to(tdt).double()
-    # one unit in the last place of the rounded value; fp16 steps never go below 2^-24
-    # (subnormals), bf16 keeps the fp32 exponent range
-    mant, floor = (10, 2.0 ** -24) if dtype == "f16" else (7, 2.0 ** -133)
-    ulp = (ref_r.abs().clamp_min(1e-38).log2().floor() - mant).exp2().clamp_min(floor)
-    excess = ((got - ref_r).abs() - ulp).max().item()
+    got = run_decode(P, w, out_dtype=tdt, partition_size=512)
+    ref = oracle_decode(w)
+    assert max_abs(got, ref) <= TOL[dtype]
+    excess = _ulp_excess(got, ref, dtype)
     assert excess <= 0, "worst excess over one ulp: %g" % excess
 
 
@@ -457,23 +453,25 @@ def test_multi_query_decode_matches_oracle(P, dtype, Hq, Hkv, D, B, ctx, nq, psi
 
 # ------------------------------------------------------------------ exactly what bench.py times
 
-def _ulp_excess(got, ref, dtype, ulps=1):
+def _ulp_excess(got, ref, dtype, ulps=1, abs_floor=1e-5):
     """How far the 16-bit output lies beyond `ulps` units in the last place of the oracle
-    rounded to that type (<= 0: within)."""
+    rounded to that type, plus `abs_floor` (<= 0: within).  The floor covers outputs near
+    zero, whose units in the last place are far below the fp32 accumulation error, which
+    scales with the terms summed, not with their (cancelling) sum."""
     tdt = workloads.TORCH_DTYPE[dtype]
     ref_t = torch.from_numpy(ref)
     ref_r = ref_t.to(tdt).double()
     mant, floor = (10, 2.0 ** -24) if dtype == "f16" else (7, 2.0 ** -133)
     ulp = (ref_r.abs().clamp_min(1e-38).log2().floor() - mant).exp2().clamp_min(floor)
-    return ((got.double().cpu() - ref_r).abs() - ulps * ulp).max().item()
+    return ((got.double().cpu() - ref_r).abs() - ulps * ulp - abs_floor).max().item()
 
 
 @pytest.mark.parametrize("name", ["llama13b_b16", "gqa_prefix", "long_splitk"])
 def test_bench_step_matches_oracle_at_full_size(P, name):
     """bench.py's own Step (fused append + decode, output in the pool type, the partition
     size and engine it uses) on the full batch: slots and pools bit-exact; the output within
-    the stated 2e-3 of the unrounded oracle, and within two units in the last place of the
-    oracle rounded to the output type (sampled sequences for the long contexts)."""
+    the stated 2e-3 of the unrounded oracle, and within one unit in the last place (+1e-5)
+    of the oracle rounded to the output type (sampled sequences for the long contexts)."""
     import bench
     w = workloads.make(name, seed=0, device=DEV)
     st = bench.Step(P, w, torch.device(DEV), fused=True)
@@ -498,5 +496,5 @@ def test_bench_step_matches_oracle_at_full_size(P, name):
     got = st.out[torch.as_tensor(seqs, device=DEV)]
     assert got.dtype == w.q.dtype
     assert max_abs(got, ref) <= TOL[w.dtype]
-    assert _ulp_excess(got, ref, w.dtype, ulps=2) <= 0
+    assert _ulp_excess(got, ref, w.dtype) <= 0
     assert_no_device_error(P)
