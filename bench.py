@@ -4,8 +4,9 @@ A step is the whole paged decode path for one batch: slot mapping of each
 sequence's new token, the cache write of its K/V rows, paged attention decode
 (partitioned with the log-sum-exp merge where the lengths call for it) and,
 on batches that share prefix blocks, the copy-on-write block copy.  Inputs are
-resident in HBM; the L2 is flushed (a 256 MiB write) before every timed step,
-outside the timed events.
+resident in HBM; consecutive timed steps read two KV pools of the batch's shape
+(two layers' caches, each larger than L2), so every step is L2-cold (--l2 flush
+writes 256 MiB before each step instead).
 
 Prints one JSON line.  value = algorithmic bytes of the step / step time (GB/s);
 tokens/s/layer = sequences / step time.  --impl reference times the CPU oracle
@@ -270,11 +271,25 @@ def run_ours(args):
 
     w = workloads.make(args.workload, seed=args.seed + rank, device=device)
     st = Step(P, w, device, fused=not args.unfused)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    # Keep every timed step L2-cold: by default consecutive steps read two KV pools of the
+    # batch's shape (two layers' caches, each larger than L2); --l2 flush instead writes
+    # 256 MiB before each step (outside the events), which leaves dirty lines in L2 that the
+    # timed step then has to write back.
+    # (a pool smaller than twice the L2 is flushed instead: alternating would not evict it)
+    l2_mode = args.l2 if 2 * (w.k_pool.nbytes + w.v_pool.nbytes) > FLUSH_BYTES else "flush"
+    pools = [(w.k_pool, w.v_pool), (w.k_pool.clone(), w.v_pool.clone())]
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device) if l2_mode == "flush" else None
     stream = torch.cuda.current_stream(device)
 
-    for _ in range(args.warmup):
-        flush.zero_()
+    def prepare(i):
+        if flush is not None:
+            flush.zero_()
+            w.k_pool, w.v_pool = pools[0]
+        else:
+            w.k_pool, w.v_pool = pools[i % 2]
+
+    for i in range(args.warmup):
+        prepare(i)
         st.pre_decode()
         st.decode()
     torch.cuda.synchronize(device)
@@ -287,7 +302,7 @@ def run_ours(args):
     with ClockSampler(device.index) as clocks:
         t_wall = time.perf_counter()
         for i in range(args.steps):
-            flush.zero_()
+            prepare(i)
             e0, e1, e2 = evs[i]
             e0.record(stream)
             st.pre_decode()
@@ -304,7 +319,8 @@ def run_ours(args):
         raise RuntimeError("device error flags set during the timed steps")
 
     # end to end through the binding with host buffers: H2D inputs, the step, D2H output
-    e2e = run_e2e(P, w, st, args, device, flush)
+    e2e = run_e2e(P, w, st, args, device, pools)
+    w.k_pool, w.v_pool = pools[0]
     e2e_ms_max = max_over_ranks(e2e["ms"], world, device)
 
     dec_logical, dec_unique, other = step_bytes(w, st.psize if st.split else 0)
@@ -356,7 +372,9 @@ def run_ours(args):
             "pool_blocks": w.num_blocks,
             "kv_bytes_per_step": int(w.context_lens.sum()) * accounting.kv_bytes_per_token(
                 w.num_kv_heads, w.head_dim, workloads.ELEM_BYTES[w.dtype]),
-            "l2": "flushed by a 256 MiB write before every timed step (outside the events)",
+            "l2": ("consecutive steps alternate between two KV pools of this shape (two layers' "
+                   "caches, each larger than L2)" if l2_mode == "alternate" else
+                   "flushed by a 256 MiB write before every timed step (outside the events)"),
             "parallelism": "replicas, one batch per GPU" if world > 1 else "single GPU",
             "seed": args.seed,
             "path": ("decode with the append fused (slot, write, attention in one launch)"
@@ -381,7 +399,7 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
 
 
-def run_e2e(P, w, st, args, device, flush):
+def run_e2e(P, w, st, args, device, pools):
     """The same step end to end through the binding: every step copies its inputs (q, new
     K/V rows, block tables, positions, lengths) from pinned host memory and reads its output
     back.  As a serving loop would, the copies run on their own stream two steps deep: step
@@ -403,7 +421,6 @@ def run_e2e(P, w, st, args, device, flush):
     in_ready = [torch.cuda.Event() for _ in range(2)]
     computed = [torch.cuda.Event() for _ in range(2)]
     out_read = [torch.cuda.Event() for _ in range(2)]
-    pools = [(w.k_pool, w.v_pool), (w.k_pool.clone(), w.v_pool.clone())]
     saved = (w.q, w.k_new, w.v_new, st.bt, st.pos, st.ctx, st.out, w.k_pool, w.v_pool)
 
     def load(i):
@@ -447,7 +464,6 @@ def run_e2e(P, w, st, args, device, flush):
         ms = run(max(3, args.steps // 4))
     finally:
         w.q, w.k_new, w.v_new, st.bt, st.pos, st.ctx, st.out, w.k_pool, w.v_pool = saved
-        del pools
     return {"ms": ms, "h2d": h2d, "d2h": d2h}
 
 
@@ -519,6 +535,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.CONFIGS))
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--l2", choices=["alternate", "flush"], default="alternate",
+                    help="how timed steps are kept L2-cold")
     ap.add_argument("--unfused", action="store_true",
                     help="slot mapping, cache write and decode as three launches")
     args = ap.parse_args()
