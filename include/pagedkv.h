@@ -53,6 +53,7 @@ typedef enum pkv_dtype { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2 } pkv_dtype;
 #define PKV_DEVERR_TIMEOUT  0x8u  /* a copy pipeline wait ran out of time (about 2 s) */
 #define PKV_DEVERR_POSITION 0x10u /* slot mapping: position past the table row, or bad sequence index */
 #define PKV_DEVERR_PAIR     0x20u /* copy_blocks: a src or dst outside [0, num_blocks) */
+#define PKV_DEVERR_PREFIX   0x40u /* cascade decode: a sequence's prefix blocks differ from sequence 0's */
 
 /*
  * The physical block pool: two caller-owned device arrays, K and V, each laid
@@ -209,6 +210,37 @@ pkv_status pkv_paged_attention_decode_multi(
     const int32_t* context_lens, int32_t max_context_len, float scale, void* out,
     int32_t out_dtype, int32_t partition_size, void* workspace, size_t workspace_bytes,
     void* stream);
+
+/*
+ * Decode for a batch whose sequences all begin with the same prefix_len tokens
+ * held in the same physical blocks (a shared system prompt: "Serving models
+ * with vLLM", section "How it works: PagedAttention": requests with the same
+ * prefix point at the same physical blocks).  Same result as
+ * pkv_paged_attention_decode (or, with k_new / v_new, as
+ * pkv_paged_attention_decode_append), computed in three launches: attention of
+ * all sequences' queries over the shared prefix, read once per kv head and run
+ * on tensor cores; the paged decode of each sequence's own positions
+ * [prefix_len, context_lens[s]) in partitions of partition_size (0 =
+ * automatic); and the log-sum-exp merge of the two.
+ *   prefix_len   > 0, a multiple of 16 and of block_size, <= every context length;
+ *                the first prefix_len / B table entries of every sequence must equal
+ *                sequence 0's (checked on the device: PKV_DEVERR_PREFIX)
+ *   k_new, v_new optional ([num_seqs][num_kv_heads][head_dim]): append each
+ *                sequence's new token at position context_lens[s] - 1 (which must
+ *                lie past the prefix) as the fused entry point does; NULL for none
+ *   slot_mapping optional output as in pkv_paged_attention_decode_append
+ *   workspace    pkv_cascade_workspace_bytes(...) bytes, always required
+ * fp16 / bf16 pools only (PKV_ERR_UNSUPPORTED for fp32).
+ */
+size_t pkv_cascade_workspace_bytes(const pkv_pool* pool, int32_t num_seqs, int32_t num_q_heads,
+                                   int32_t max_context_len, int32_t prefix_len,
+                                   int32_t partition_size);
+pkv_status pkv_paged_attention_decode_cascade(
+    const pkv_pool* pool, const void* q, int32_t num_seqs, int32_t num_q_heads,
+    const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* context_lens,
+    int32_t max_context_len, float scale, int32_t prefix_len, void* out, int32_t out_dtype,
+    int32_t partition_size, const void* k_new, const void* v_new, int64_t* slot_mapping,
+    void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * The partition step alone: for every sequence s, q head h and partition

@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "pkv_common.cuh"
+#include "prefix.cuh"
 
 namespace {
 
@@ -192,6 +193,8 @@ pkv_status run_decode(const DecodeArgs& a, void* out, int32_t out_dtype, int dir
         mp.partition_size = P;
         mp.skip_single = 1;
         mp.num_queries = a.NQ;
+        mp.prefix_parts = 0;
+        mp.skip_tokens = 0;
         mp.out = out;
         mp.out_dtype = out_dtype;
         mp.err = err;
@@ -404,6 +407,141 @@ pkv_status pkv_paged_attention_decode_multi(
                       static_cast<cudaStream_t>(stream));
 }
 
+namespace {
+
+struct CascadeShape {
+    int32_t P, suffix_parts, max_parts;
+};
+
+CascadeShape cascade_shape(const pkv_pool* pool, int32_t max_ctx, int32_t prefix_len,
+                           int32_t partition_size) {
+    const int32_t rest = max_ctx > prefix_len ? max_ctx - prefix_len : 0;
+    const int32_t P = partition_size > 0 ? partition_size : auto_partition(pool, rest);
+    const int32_t sp = rest > 0 ? ceil_div(rest, P) : 1;
+    return CascadeShape{P, sp, 1 + sp};
+}
+
+}  // namespace
+
+size_t pkv_cascade_workspace_bytes(const pkv_pool* pool, int32_t num_seqs, int32_t num_q_heads,
+                                   int32_t max_context_len, int32_t prefix_len,
+                                   int32_t partition_size) {
+    if (!pool || pool->block_size <= 0 || pool->head_dim <= 0 || num_seqs < 0 ||
+        num_q_heads <= 0 || max_context_len < 0 || prefix_len <= 0 || partition_size < 0)
+        return 0;
+    const CascadeShape c = cascade_shape(pool, max_context_len, prefix_len, partition_size);
+    return ws_layout(num_seqs, num_q_heads, pool->head_dim, c.max_parts).bytes;
+}
+
+pkv_status pkv_paged_attention_decode_cascade(
+    const pkv_pool* pool, const void* q, int32_t num_seqs, int32_t num_q_heads,
+    const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* context_lens,
+    int32_t max_context_len, float scale, int32_t prefix_len, void* out, int32_t out_dtype,
+    int32_t partition_size, const void* k_new, const void* v_new, int64_t* slot_mapping,
+    void* workspace, size_t workspace_bytes, void* stream) {
+    DecodeArgs a{pool, q, num_seqs, num_q_heads, block_tables, max_blocks_per_seq,
+                 context_lens, max_context_len, scale, partition_size};
+    pkv_status st = check_decode(a);
+    if (st != PKV_OK) return st;
+    if (pool->dtype == PKV_F32) return PKV_ERR_UNSUPPORTED;
+    if (out_dtype != PKV_F32 && out_dtype != pool->dtype) return PKV_ERR_UNSUPPORTED;
+    if (prefix_len <= 0 || prefix_len % 16 != 0 || prefix_len % pool->block_size != 0 ||
+        prefix_len > max_context_len || (int64_t)prefix_len > (int64_t)max_blocks_per_seq * pool->block_size)
+        return PKV_ERR_INVALID;
+    if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_INVALID;
+    if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return PKV_ERR_INVALID;
+    if (num_seqs > 0 && !out) return PKV_ERR_INVALID;
+    const CascadeShape c = cascade_shape(pool, max_context_len, prefix_len, partition_size);
+    if (c.suffix_parts > 65535) return PKV_ERR_UNSUPPORTED;
+    const WsLayout lay = ws_layout(num_seqs, num_q_heads, pool->head_dim, c.max_parts);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < lay.bytes) return PKV_ERR_WORKSPACE;
+    if (num_seqs == 0) return PKV_OK;
+    unsigned int* err = nullptr;
+    st = error_word(&err);
+    if (st != PKV_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* ws = static_cast<char*>(workspace);
+    float* ws_m = reinterpret_cast<float*>(ws);
+    float* ws_l = reinterpret_cast<float*>(ws + lay.l_off);
+    float* ws_o = reinterpret_cast<float*>(ws + lay.o_off);
+    const int G = num_q_heads / pool->num_kv_heads;
+
+    pkv::PrefixParams pp{};
+    pp.q = q;
+    pp.num_seqs = num_seqs;
+    pp.num_q_heads = num_q_heads;
+    pp.num_kv_heads = pool->num_kv_heads;
+    pp.num_blocks = pool->num_blocks;
+    pp.block_size = pool->block_size;
+    pp.block_tables = block_tables;
+    pp.max_blocks_per_seq = max_blocks_per_seq;
+    pp.prefix_len = prefix_len;
+    pp.scale_log2 = scale * 1.4426950408889634f;
+    pp.max_parts = c.max_parts;
+    pp.ws_m = ws_m;
+    pp.ws_l = ws_l;
+    pp.ws_o = ws_o;
+    pp.err = err;
+    cudaError_t e = pool->dtype == PKV_F16
+                        ? pkv::launch_prefix<__half>(pp, pool->k, pool->v, pool->head_dim, s)
+                        : pkv::launch_prefix<__nv_bfloat16>(pp, pool->k, pool->v, pool->head_dim, s);
+    if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
+
+    pkv::DecodeParams p{};
+    p.k_pool = pool->k;
+    p.v_pool = pool->v;
+    p.num_blocks = pool->num_blocks;
+    p.block_size = pool->block_size;
+    p.num_kv_heads = pool->num_kv_heads;
+    p.q = q;
+    p.num_seqs = num_seqs;
+    p.num_q_heads = num_q_heads;
+    p.block_tables = block_tables;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.context_lens = context_lens;
+    p.max_context_len = max_context_len;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.partition_size = c.P;
+    p.max_parts = c.max_parts;
+    p.out = out;
+    p.out_dtype = out_dtype;
+    p.direct_single = 0;
+    p.skip_tokens = prefix_len;
+    p.part_offset = 1;
+    p.num_queries = 1;
+    p.queries_per_cta = 1;
+    p.ws_m = ws_m;
+    p.ws_l = ws_l;
+    p.ws_o = ws_o;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.slot_out = slot_mapping;
+    p.err = err;
+    // the suffix decode's grid covers max_parts - part_offset = suffix partitions
+    if (launch_decode_typed(p, pool->dtype, pool->head_dim, G, s) != cudaSuccess)
+        return PKV_ERR_CUDA;
+
+    pkv::MergeParams mp{};
+    mp.ws_m = ws_m;
+    mp.ws_l = ws_l;
+    mp.ws_o = ws_o;
+    mp.context_lens = context_lens;
+    mp.num_seqs = num_seqs;
+    mp.num_q_heads = num_q_heads;
+    mp.head_dim = pool->head_dim;
+    mp.max_parts = c.max_parts;
+    mp.partition_size = c.P;
+    mp.skip_single = 0;
+    mp.num_queries = 1;
+    mp.prefix_parts = 1;
+    mp.skip_tokens = prefix_len;
+    mp.out = out;
+    mp.out_dtype = out_dtype;
+    mp.err = err;
+    return pkv::launch_merge(mp, s) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 pkv_status pkv_paged_attention_partitions(const pkv_pool* pool, const void* q, int32_t num_seqs,
                                           int32_t num_q_heads, const int32_t* block_tables,
                                           int32_t max_blocks_per_seq,
@@ -449,6 +587,8 @@ pkv_status pkv_lse_merge(const void* workspace, size_t workspace_bytes, int32_t 
     mp.partition_size = partition_size;
     mp.skip_single = 0;
     mp.num_queries = 1;
+    mp.prefix_parts = 0;
+    mp.skip_tokens = 0;
     mp.out = out;
     mp.out_dtype = out_dtype;
     mp.err = err;

@@ -3,6 +3,7 @@
 // heads (decode_mma.cuh), chosen by the engine setting.
 #include "decode.cuh"
 #include "decode_mma.cuh"
+#include "prefix.cuh"
 
 namespace pkv {
 
@@ -19,6 +20,12 @@ template <>
 cudaError_t launch_decode_mma<__half>(const DecodeParams& p, int head_dim, int group,
                                   cudaStream_t stream) {
     return launch_decode_mma_impl<__half>(p, head_dim, group, stream);
+}
+
+template <>
+cudaError_t launch_prefix<__half>(const PrefixParams& p, const void* k_pool, const void* v_pool,
+                               int head_dim, cudaStream_t stream) {
+    return launch_prefix_impl<__half>(p, k_pool, v_pool, head_dim, stream);
 }
 
 }  // namespace pkv

@@ -161,7 +161,8 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
     bool ctx_bad = false;
     {
         const long long cap_table = (long long)p.max_blocks_per_seq * B;
-        const long long cap_grid = (long long)p.max_parts * P;
+        const long long cap_grid =
+            (long long)p.skip_tokens + (long long)(p.max_parts - p.part_offset) * P;
         long long cap = cap_table < cap_grid ? cap_table : cap_grid;
         if (cap > p.max_context_len) cap = p.max_context_len;
         if (ctx < 0 || ctx > cap) {
@@ -170,20 +171,22 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
             ctx_bad = true;
         }
     }
-    const int n_parts = (ctx + P - 1) / P;
-    const int tok0 = part * P;
+    const int skip = p.skip_tokens;
+    const int n_parts = ctx > skip ? (ctx - skip + P - 1) / P : 0;
+    const int tok0 = skip + part * P;
     if (part > 0 && tok0 >= ctx) return;
     const bool direct = p.direct_single && n_parts <= 1;
     if ((ctx == 0 || ctx_bad) && p.slot_out && kvh == 0 && part == 0 && threadIdx.x == 0)
         p.slot_out[s] = -1;
-    if (ctx == 0) {
+    if (ctx <= skip) {  // nothing to attend to here: zero output or an empty partial
+        if (ctx < skip && threadIdx.x == 0 && blockIdx.x == 0) set_error(p.err, PKV_DEVERR_CONTEXT);
         for (int i = threadIdx.x; i < ncols * D; i += NW * 32) {
             const size_t row = col_row(i / D);
             const int d = i % D;
             if (direct) {
                 store_out(p.out, p.out_dtype, row * D + d, 0.f);
             } else {
-                const size_t r = row * p.max_parts;
+                const size_t r = row * p.max_parts + p.part_offset;
                 p.ws_o[r * D + d] = 0.f;
                 if (d == 0) { p.ws_m[r] = -INFINITY; p.ws_l[r] = 0.f; }
             }
@@ -444,7 +447,7 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
         if (direct) {
             store_out(p.out, p.out_dtype, row * D + d, L > 0.f ? O / L : 0.f);
         } else {
-            const size_t rr = row * p.max_parts + part;
+            const size_t rr = row * p.max_parts + part + p.part_offset;
             p.ws_o[rr * D + d] = O;
             if (d == 0) {
                 p.ws_m[rr] = M * 0.69314718055994530942f;
@@ -509,7 +512,7 @@ cudaError_t launch_decode_mma_td(const DecodeParams& p, cudaStream_t stream) {
         configured[dev] = true;
     }
     const int groups = (p.num_queries + p.queries_per_cta - 1) / p.queries_per_cta;
-    dim3 grid(p.num_kv_heads * groups, p.num_seqs, p.max_parts);
+    dim3 grid(p.num_kv_heads * groups, p.num_seqs, p.max_parts - p.part_offset);
     kernel<<<grid, NW * 32, SMEM, stream>>>(tk, tv, p);
     return cudaGetLastError();
 }

@@ -128,7 +128,7 @@ cudaError_t launch_copy_blocks(const pkv_pool& src, const pkv_pool& dst, const i
 }
 
 // ------------------------------------------------------------------ log-sum-exp merge
-// Row (s, h) with n = ceil(ctx / P) partitions:  M = max_k m_k,
+// Row (s, h) with n = prefix_parts + ceil((ctx - skip_tokens) / P) partitions:  M = max_k m_k,
 // out = sum_k e^(m_k - M) o_k / sum_k e^(m_k - M) l_k.  One CTA (4 warps) per row;
 // warp w takes partitions k = w, w + 4, ...; lane j holds dims j, j + 32, ...
 template <int D>
@@ -143,10 +143,12 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(const MergeParams p) {
     const int s = row / (p.num_q_heads * p.num_queries);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int ctx = p.context_lens[s];
-    const long long cap = (long long)p.max_parts * p.partition_size;
+    const long long cap = (long long)p.skip_tokens +
+                          (long long)(p.max_parts - p.prefix_parts) * p.partition_size;
     if (ctx < 0) ctx = 0;
     if (ctx > cap) ctx = int(cap);
-    const int n = (ctx + p.partition_size - 1) / p.partition_size;
+    const int rest = ctx > p.skip_tokens ? ctx - p.skip_tokens : 0;
+    const int n = p.prefix_parts + (rest + p.partition_size - 1) / p.partition_size;
     if (p.skip_single && n <= 1) return;
     const float* mrow = p.ws_m + (size_t)row * p.max_parts;
     const float* lrow = p.ws_l + (size_t)row * p.max_parts;

@@ -39,6 +39,8 @@ struct DecodeParams {
     void* out;
     int32_t out_dtype;
     int32_t direct_single;  // 1: sequences with one partition write out directly
+    int32_t skip_tokens;    // attend to positions >= skip_tokens only (0: the whole context)
+    int32_t part_offset;    // partition k writes workspace slot k + part_offset
     int32_t num_queries;    // query rows per sequence (1 for decode)
     int32_t queries_per_cta;  // tensor-core kernel: queries sharing one CTA's 8 columns
     float* ws_m;
@@ -65,6 +67,8 @@ struct MergeParams {
     int32_t partition_size;
     int32_t skip_single;    // 1: rows with <= 1 partition were written by the decode kernel
     int32_t num_queries;    // rows are [num_seqs][num_queries][num_q_heads]
+    int32_t prefix_parts;   // slots before the context's partitions (1: a shared-prefix partial)
+    int32_t skip_tokens;    // the partitions cover positions >= skip_tokens
     void* out;
     int32_t out_dtype;
     unsigned int* err;
@@ -222,6 +226,11 @@ template <typename T>
 cudaError_t launch_decode_mma(const DecodeParams& p, int head_dim, int group, cudaStream_t stream);
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
+struct PrefixParams;
+// attention over a shared prefix into workspace slot 0 (16-bit pools, prefix.cuh)
+template <typename T>
+cudaError_t launch_prefix(const PrefixParams& p, const void* k_pool, const void* v_pool,
+                          int head_dim, cudaStream_t stream);
 cudaError_t launch_slot_mapping(const int32_t* block_tables, int32_t max_blocks_per_seq,
                                 int32_t num_seqs, const int32_t* positions,
                                 const int32_t* token_seq, int32_t num_tokens, int32_t block_size,

@@ -25,7 +25,7 @@ lib = ctypes.CDLL(LIB_PATH)
 PKV_OK, PKV_ERR_INVALID, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_ERR_CUDA, PKV_ERR_DEVICE = range(6)
 PKV_F32, PKV_F16, PKV_BF16 = 0, 1, 2
 DEVERR = {"BLOCK_ID": 0x1, "SLOT": 0x2, "CONTEXT": 0x4, "TIMEOUT": 0x8, "POSITION": 0x10,
-          "PAIR": 0x20}
+          "PAIR": 0x20, "PREFIX": 0x40}
 
 _DTYPE = {torch.float32: PKV_F32, torch.float16: PKV_F16, torch.bfloat16: PKV_BF16}
 
@@ -58,6 +58,9 @@ _SIGS = {
                                                  _f32, _P, _i32, _i32, _P, _sz, _P, _P]),
     "pkv_paged_attention_decode_multi": (_i32, [_PP, _P, _i32, _i32, _i32, _P, _i32, _P, _i32,
                                                 _f32, _P, _i32, _i32, _P, _sz, _P]),
+    "pkv_cascade_workspace_bytes": (_sz, [_PP, _i32, _i32, _i32, _i32, _i32]),
+    "pkv_paged_attention_decode_cascade": (_i32, [_PP, _P, _i32, _i32, _P, _i32, _P, _i32, _f32,
+                                                  _i32, _P, _i32, _i32, _P, _P, _P, _P, _sz, _P]),
     "pkv_paged_attention_partitions": (_i32, [_PP, _P, _i32, _i32, _P, _i32, _P, _i32, _f32, _i32,
                                               _P, _sz, _P]),
     "pkv_lse_merge": (_i32, [_P, _sz, _i32, _i32, _i32, _P, _i32, _i32, _P, _i32, _P]),
@@ -222,6 +225,28 @@ def pkv_paged_attention_decode_multi(q, k_pool, v_pool, block_tables, context_le
         _ptr(context_lens), int(max_context_len), float(scale), _ptr(out), _DTYPE[out.dtype],
         int(partition_size), _ptr(workspace), ws_bytes, _stream(stream, q)),
         "pkv_paged_attention_decode_multi")
+
+
+def pkv_cascade_workspace_bytes(k_pool, num_seqs, num_q_heads, max_context_len, prefix_len,
+                                partition_size=0):
+    pool = make_pool(k_pool, k_pool)
+    return lib.pkv_cascade_workspace_bytes(ctypes.byref(pool), num_seqs, num_q_heads,
+                                           max_context_len, prefix_len, partition_size)
+
+
+def pkv_paged_attention_decode_cascade(q, k_pool, v_pool, block_tables, context_lens, scale, out,
+                                       max_context_len, prefix_len, workspace, partition_size=0,
+                                       k_new=None, v_new=None, slot_mapping=None, stream=None):
+    """Decode for a batch whose sequences all share their first prefix_len tokens' blocks."""
+    _contig(q, block_tables, context_lens, out, workspace, k_new, v_new, slot_mapping)
+    pool = make_pool(k_pool, v_pool)
+    S, Hq, _ = q.shape
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib.pkv_paged_attention_decode_cascade(
+        ctypes.byref(pool), _ptr(q), S, Hq, _ptr(block_tables), block_tables.shape[1],
+        _ptr(context_lens), int(max_context_len), float(scale), int(prefix_len), _ptr(out),
+        _DTYPE[out.dtype], int(partition_size), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
+        _ptr(workspace), ws_bytes, _stream(stream, q)), "pkv_paged_attention_decode_cascade")
 
 
 def pkv_paged_attention_decode_static_workspace(q, k_pool, v_pool, block_tables, context_lens,

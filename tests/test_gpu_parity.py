@@ -110,10 +110,7 @@ def test_16bit_output_is_oracle_rounded_within_one_ulp(P, engine, dtype):
                         block_size=16, context_lens=[7, 300, 1500], seed=5, device=DEV)
     tdt = workloads.TORCH_DTYPE[dtype]
     got = run_decode(P, w, out_dtype=tdt, partition_size=512)
-    ref = oracle_decode(w)
-    assert max_abs(got, ref) <= TOL[dtype]
-    excess = _ulp_excess(got, ref, dtype)
-    assert excess <= 0, "worst excess over one ulp: %g" % excess
+    _assert_16bit_close(got, oracle_decode(w), dtype)
 
 
 @pytest.mark.parametrize("engine", [1, 2], ids=["cuda_cores", "tensor_cores"], indirect=True)
@@ -453,6 +450,19 @@ def test_multi_query_decode_matches_oracle(P, dtype, Hq, Hkv, D, B, ctx, nq, psi
 
 # ------------------------------------------------------------------ exactly what bench.py times
 
+def _assert_16bit_close(got, ref, dtype):
+    """A 16-bit output: within the stated tolerance of the unrounded oracle plus half a unit
+    in the last place of the output type (the rounding of the result itself), and within
+    one unit of the oracle rounded to that type."""
+    tdt = workloads.TORCH_DTYPE[dtype]
+    ref_r = torch.from_numpy(ref).to(tdt).double()
+    mant, floor = (10, 2.0 ** -24) if dtype == "f16" else (7, 2.0 ** -133)
+    ulp = (ref_r.abs().clamp_min(1e-38).log2().floor() - mant).exp2().clamp_min(floor)
+    err = (got.double().cpu() - torch.from_numpy(ref)).abs() - 0.5 * ulp
+    assert err.max().item() <= TOL[dtype], err.max().item()
+    assert _ulp_excess(got, ref, dtype) <= 0
+
+
 def _ulp_excess(got, ref, dtype, ulps=1, abs_floor=1e-5):
     """How far the 16-bit output lies beyond `ulps` units in the last place of the oracle
     rounded to that type, plus `abs_floor` (<= 0: within).  The floor covers outputs near
@@ -469,9 +479,10 @@ def _ulp_excess(got, ref, dtype, ulps=1, abs_floor=1e-5):
 @pytest.mark.parametrize("name", ["llama13b_b16", "gqa_prefix", "long_splitk"])
 def test_bench_step_matches_oracle_at_full_size(P, name):
     """bench.py's own Step (fused append + decode, output in the pool type, the partition
-    size and engine it uses) on the full batch: slots and pools bit-exact; the output within
-    the stated 2e-3 of the unrounded oracle, and within one unit in the last place (+1e-5)
-    of the oracle rounded to the output type (sampled sequences for the long contexts)."""
+    size and engine it uses) on the full batch: slots and pools bit-exact; the 16-bit output
+    within the stated 2e-3 (plus its own rounding) of the unrounded oracle and within one
+    unit in the last place of the oracle rounded to the output type (sampled sequences for
+    the long contexts)."""
     import bench
     w = workloads.make(name, seed=0, device=DEV)
     st = bench.Step(P, w, torch.device(DEV), fused=True)
@@ -495,6 +506,69 @@ def test_bench_step_matches_oracle_at_full_size(P, name):
                                   w.block_tables, w.context_lens, w.scale)
     got = st.out[torch.as_tensor(seqs, device=DEV)]
     assert got.dtype == w.q.dtype
-    assert max_abs(got, ref) <= TOL[w.dtype]
-    assert _ulp_excess(got, ref, w.dtype) <= 0
+    _assert_16bit_close(got, ref, w.dtype)
     assert_no_device_error(P)
+
+
+# ------------------------------------------------------------------ shared-prefix (cascade) decode
+
+@pytest.mark.parametrize("dtype,Hq,Hkv,D,B,prefix_blocks,suffix,psize", [
+    ("bf16", 32, 8, 128, 16, 4, [1, 30, 700, 2000, 16], 0),     # tensor-core suffix, G = 4
+    ("f16", 8, 8, 128, 32, 3, [5, 64, 1100, 33], 512),         # CUDA-core suffix (MHA), B = 32
+    ("f16", 16, 2, 64, 16, 2, [0, 9, 300], 256),               # a sequence that is all prefix
+])
+def test_cascade_decode_matches_oracle_and_plain_decode(P, dtype, Hq, Hkv, D, B, prefix_blocks,
+                                                        suffix, psize):
+    Lp = prefix_blocks * B
+    ctx = [Lp + x for x in suffix]
+    w = workloads.build("cascade", dtype=dtype, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                        block_size=B, context_lens=ctx, seed=51, device=DEV,
+                        shared_prefix_blocks=prefix_blocks)
+    mcl = w.max_context_len
+    ws = P.workspace_tensor(P.pkv_cascade_workspace_bytes(w.k_pool, w.num_seqs, Hq, mcl, Lp,
+                                                          psize), DEV)
+    out = torch.full((w.num_seqs, Hq, D), float("nan"), dtype=torch.float32, device=DEV)
+    P.pkv_paged_attention_decode_cascade(w.q, w.k_pool, w.v_pool, dev_i32(w.block_tables),
+                                         dev_i32(w.context_lens), w.scale, out, mcl, Lp, ws,
+                                         psize)
+    torch.cuda.synchronize()
+    ref = oracle_decode(w)
+    assert max_abs(out, ref) <= TOL[dtype]
+    plain = run_decode(P, w, partition_size=psize)
+    assert max_abs(out, plain.double().cpu().numpy()) <= 1e-5
+    assert_no_device_error(P)
+
+
+def test_cascade_with_fused_append_matches_oracle(P):
+    w = workloads.build("cascade_app", dtype="bf16", num_q_heads=32, num_kv_heads=8, head_dim=128,
+                        block_size=16, context_lens=[100, 600, 1500, 65], seed=52, device=DEV,
+                        shared_prefix_blocks=4)
+    Lp, mcl = 64, w.max_context_len
+    k0, v0 = host(w.k_pool).copy(), host(w.v_pool).copy()
+    ws = P.workspace_tensor(P.pkv_cascade_workspace_bytes(w.k_pool, w.num_seqs, 32, mcl, Lp), DEV)
+    out = torch.empty((w.num_seqs, 32, 128), dtype=torch.bfloat16, device=DEV)
+    slots = torch.empty(w.num_seqs, dtype=torch.int64, device=DEV)
+    P.pkv_paged_attention_decode_cascade(w.q, w.k_pool, w.v_pool, dev_i32(w.block_tables),
+                                         dev_i32(w.context_lens), w.scale, out, mcl, Lp, ws,
+                                         k_new=w.k_new, v_new=w.v_new, slot_mapping=slots)
+    torch.cuda.synchronize()
+    ref_slots = oracle.slot_mapping(w.block_tables, w.positions, 16)
+    assert np.array_equal(slots.cpu().numpy(), ref_slots)
+    oracle.kv_cache_write("bf16", k0, v0, host(w.k_new), host(w.v_new), ref_slots)
+    assert np.array_equal(host(w.k_pool), k0) and np.array_equal(host(w.v_pool), v0)
+    ref = oracle.paged_decode("bf16", k0, v0, host(w.q), w.block_tables, w.context_lens, w.scale)
+    _assert_16bit_close(out, ref, "bf16")
+    assert_no_device_error(P)
+
+
+def test_cascade_flags_a_sequence_with_other_prefix_blocks(P):
+    w = workloads.build("cascade_bad", dtype="f16", num_q_heads=8, num_kv_heads=2, head_dim=128,
+                        block_size=16, context_lens=[80, 90, 100], seed=53, device=DEV,
+                        shared_prefix_blocks=2)
+    bt = w.block_tables.copy()
+    bt[2, 1] = bt[2, 3]                                     # sequence 2 no longer shares block 1
+    ws = P.workspace_tensor(P.pkv_cascade_workspace_bytes(w.k_pool, 3, 8, 100, 32), DEV)
+    out = torch.empty((3, 8, 128), dtype=torch.float32, device=DEV)
+    P.pkv_paged_attention_decode_cascade(w.q, w.k_pool, w.v_pool, dev_i32(bt),
+                                         dev_i32(w.context_lens), w.scale, out, 100, 32, ws)
+    assert P.pkv_get_device_error() & P.DEVERR["PREFIX"]
