@@ -167,8 +167,12 @@ def max_over_ranks(x, world, device):
 class Step:
     """Device buffers and the launch sequence of one decode step through the binding."""
 
-    def __init__(self, P, w, device, fused=True):
+    def __init__(self, P, w, device, fused=True, cascade=True):
         self.P, self.w, self.dev, self.fused = P, w, device, fused
+        # batches whose sequences share prefix blocks: the prefix's attention once per kv
+        # head on tensor cores, then each sequence's own suffix, then the merge
+        self.prefix_len = (len(w.shared_blocks) * w.block_size
+                           if cascade and len(w.shared_blocks) and w.dtype != "f32" else 0)
         i32 = lambda a: torch.as_tensor(np.ascontiguousarray(a, np.int32), device=device)
         self.bt = i32(w.block_tables)
         self.pos = i32(w.positions)
@@ -180,12 +184,20 @@ class Step:
         self.mcl = w.max_context_len
         self.psize = w.partition_size or P.pkv_choose_partition_size(
             w.k_pool, w.num_seqs, w.num_q_heads, self.mcl)
-        nbytes = P.pkv_decode_workspace_bytes(w.k_pool, w.num_seqs, w.num_q_heads, self.mcl,
-                                              self.psize)
+        if self.prefix_len:
+            self.psize = w.partition_size
+            nbytes = P.pkv_cascade_workspace_bytes(w.k_pool, w.num_seqs, w.num_q_heads, self.mcl,
+                                                   self.prefix_len, self.psize)
+        else:
+            nbytes = P.pkv_decode_workspace_bytes(w.k_pool, w.num_seqs, w.num_q_heads, self.mcl,
+                                                  self.psize)
         self.ws = P.workspace_tensor(nbytes, device) if nbytes else None
         self.split = nbytes > 0
-        self.launches = ((1 if fused else 3) + (1 if self.split else 0)
-                         + (1 if self.pairs is not None else 0))
+        if self.prefix_len:
+            self.launches = 3 + (0 if fused else 2) + (1 if self.pairs is not None else 0)
+        else:
+            self.launches = ((1 if fused else 3) + (1 if self.split else 0)
+                             + (1 if self.pairs is not None else 0))
 
     def pre_decode(self):
         """Work before the decode call: the copy-on-write copy, and unless the append is
@@ -201,7 +213,12 @@ class Step:
         """The decode call; fused: it also computes each new token's slot and writes its
         K/V rows (one launch instead of three, same result)."""
         P, w = self.P, self.w
-        if self.fused:
+        if self.prefix_len:
+            app = dict(k_new=w.k_new, v_new=w.v_new, slot_mapping=self.slots) if self.fused else {}
+            P.pkv_paged_attention_decode_cascade(w.q, w.k_pool, w.v_pool, self.bt, self.ctx,
+                                                 w.scale, self.out, self.mcl, self.prefix_len,
+                                                 self.ws, self.psize, **app)
+        elif self.fused:
             P.pkv_paged_attention_decode_append(w.q, w.k_pool, w.v_pool, w.k_new, w.v_new, self.bt,
                                                 self.ctx, w.scale, self.out, self.mcl, self.psize,
                                                 self.ws, slot_mapping=self.slots)
@@ -270,7 +287,7 @@ def run_ours(args):
     from paged_kv_cache_293_gb300 import pagedkv as P
 
     w = workloads.make(args.workload, seed=args.seed + rank, device=device)
-    st = Step(P, w, device, fused=not args.unfused)
+    st = Step(P, w, device, fused=not args.unfused, cascade=not args.no_cascade)
     # Keep every timed step L2-cold: by default consecutive steps read two KV pools of the
     # batch's shape (two layers' caches, each larger than L2); --l2 flush instead writes
     # 256 MiB before each step (outside the events), which leaves dirty lines in L2 that the
@@ -323,7 +340,14 @@ def run_ours(args):
     w.k_pool, w.v_pool = pools[0]
     e2e_ms_max = max_over_ranks(e2e["ms"], world, device)
 
-    dec_logical, dec_unique, other = step_bytes(w, st.psize if st.split else 0)
+    dec_logical, dec_unique, other = step_bytes(w, st.psize if st.split and not st.prefix_len else 0)
+    if st.prefix_len:  # the cascade's partials: a prefix slot per row plus the suffix partitions
+        p_suffix = st.psize or P.pkv_choose_partition_size(w.k_pool, w.num_seqs, w.num_q_heads,
+                                                           st.mcl - st.prefix_len)
+        extra = accounting.cascade_workspace_bytes(w.context_lens, st.prefix_len, p_suffix,
+                                                   w.num_q_heads, w.head_dim)
+        dec_logical += extra
+        dec_unique += extra
     if st.fused:  # the decode launch also reads the new rows and writes them into the pool
         dec_unique += accounting.write_bytes(w.num_seqs, w.num_kv_heads, w.head_dim,
                                              workloads.ELEM_BYTES[w.dtype])
@@ -336,6 +360,8 @@ def run_ours(args):
               and P.pkv_get_decode_engine() == P.ENGINE_AUTO)
     kernel_name = ("paged_decode_mma_kernel" if tensor else "paged_decode_kernel") + (
         " + lse_merge_kernel" if st.split else "")
+    if st.prefix_len:
+        kernel_name = "prefix_attention_kernel + " + kernel_name
 
     if rank != 0:
         return
@@ -378,7 +404,9 @@ def run_ours(args):
             "parallelism": "replicas, one batch per GPU" if world > 1 else "single GPU",
             "seed": args.seed,
             "path": ("decode with the append fused (slot, write, attention in one launch)"
-                     if st.fused else "slot mapping, cache write, decode: three launches"),
+                     if st.fused else "slot mapping, cache write, decode: three launches")
+                    + ("; cascade over the %d-token shared prefix" % st.prefix_len
+                       if st.prefix_len else ""),
         },
         "roofline": {
             "kernel": kernel_name,
@@ -537,6 +565,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--l2", choices=["alternate", "flush"], default="alternate",
                     help="how timed steps are kept L2-cold")
+    ap.add_argument("--no-cascade", action="store_true",
+                    help="shared-prefix batches: plain paged decode instead of the cascade")
     ap.add_argument("--unfused", action="store_true",
                     help="slot mapping, cache write and decode as three launches")
     args = ap.parse_args()

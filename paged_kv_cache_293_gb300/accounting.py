@@ -50,3 +50,12 @@ def copy_bytes(num_pairs, num_kv_heads, block_size, head_dim, elem_bytes):
     """Each pair reads and writes one whole block of both pools."""
     blk = num_kv_heads * block_size * head_dim * elem_bytes
     return num_pairs * (2 * 2 * blk + 8)
+
+
+def cascade_workspace_bytes(context_lens, prefix_len, partition_size, num_q_heads, head_dim):
+    """fp32 partials a cascade call writes and reads back: one prefix slot per (sequence,
+    q head) row plus one per partition of each sequence's own suffix."""
+    ctx = np.asarray(context_lens, dtype=np.int64)
+    rest = np.maximum(ctx - int(prefix_len), 0)
+    parts = 1 + (-(-rest // int(partition_size)))
+    return 2 * int(parts.sum()) * num_q_heads * (head_dim + 2) * 4
