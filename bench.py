@@ -287,7 +287,7 @@ def run_ours(args):
     from paged_kv_cache_293_gb300 import pagedkv as P
 
     w = workloads.make(args.workload, seed=args.seed + rank, device=device)
-    st = Step(P, w, device, fused=not args.unfused, cascade=not args.no_cascade)
+    st = Step(P, w, device, fused=not args.unfused, cascade=args.cascade)
     # Keep every timed step L2-cold: by default consecutive steps read two KV pools of the
     # batch's shape (two layers' caches, each larger than L2); --l2 flush instead writes
     # 256 MiB before each step (outside the events), which leaves dirty lines in L2 that the
@@ -565,8 +565,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--l2", choices=["alternate", "flush"], default="alternate",
                     help="how timed steps are kept L2-cold")
-    ap.add_argument("--no-cascade", action="store_true",
-                    help="shared-prefix batches: plain paged decode instead of the cascade")
+    ap.add_argument("--cascade", action="store_true",
+                    help="shared-prefix batches: prefix attention once per kv head, then the "
+                         "suffixes, then the merge (slower than plain decode on the batches here)")
     ap.add_argument("--unfused", action="store_true",
                     help="slot mapping, cache write and decode as three launches")
     args = ap.parse_args()
