@@ -3,6 +3,7 @@
 // Host-side argument checks, the choice of partition size, workspace layout,
 // dispatch to the typed kernels, and the device error word.  Nothing here
 // allocates device memory or synchronises, except pkv_get_device_error.
+#include <algorithm>
 #include <atomic>
 #include <climits>
 #include <cmath>
@@ -410,15 +411,23 @@ pkv_status pkv_paged_attention_decode_multi(
 namespace {
 
 struct CascadeShape {
-    int32_t P, suffix_parts, max_parts;
+    int32_t P, suffix_parts, prefix_splits, chunks_per_split, max_parts;
 };
 
-CascadeShape cascade_shape(const pkv_pool* pool, int32_t max_ctx, int32_t prefix_len,
-                           int32_t partition_size) {
+// The prefix pass is split along the prefix so that it has about 4 CTAs per SM
+// (152 SMs); each split writes one slot, followed by the suffix partitions.
+CascadeShape cascade_shape(const pkv_pool* pool, int32_t num_seqs, int32_t num_q_heads,
+                           int32_t max_ctx, int32_t prefix_len, int32_t partition_size) {
     const int32_t rest = max_ctx > prefix_len ? max_ctx - prefix_len : 0;
     const int32_t P = partition_size > 0 ? partition_size : auto_partition(pool, rest);
     const int32_t sp = rest > 0 ? ceil_div(rest, P) : 1;
-    return CascadeShape{P, sp, 1 + sp};
+    const int32_t G = num_q_heads / pool->num_kv_heads;
+    const int64_t ctas = (int64_t)pool->num_kv_heads * (((int64_t)num_seqs * G + 63) / 64);
+    const int32_t chunks = prefix_len / 16;
+    int32_t splits = (int32_t)std::min<int64_t>(chunks, std::max<int64_t>(1, (608 + ctas - 1) / std::max<int64_t>(ctas, 1)));
+    const int32_t cps = ceil_div(chunks, splits);
+    splits = ceil_div(chunks, cps);
+    return CascadeShape{P, sp, splits, cps, splits + sp};
 }
 
 }  // namespace
@@ -429,7 +438,9 @@ size_t pkv_cascade_workspace_bytes(const pkv_pool* pool, int32_t num_seqs, int32
     if (!pool || pool->block_size <= 0 || pool->head_dim <= 0 || num_seqs < 0 ||
         num_q_heads <= 0 || max_context_len < 0 || prefix_len <= 0 || partition_size < 0)
         return 0;
-    const CascadeShape c = cascade_shape(pool, max_context_len, prefix_len, partition_size);
+    if (num_q_heads % pool->num_kv_heads != 0) return 0;
+    const CascadeShape c =
+        cascade_shape(pool, num_seqs, num_q_heads, max_context_len, prefix_len, partition_size);
     return ws_layout(num_seqs, num_q_heads, pool->head_dim, c.max_parts).bytes;
 }
 
@@ -451,7 +462,8 @@ pkv_status pkv_paged_attention_decode_cascade(
     if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_INVALID;
     if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return PKV_ERR_INVALID;
     if (num_seqs > 0 && !out) return PKV_ERR_INVALID;
-    const CascadeShape c = cascade_shape(pool, max_context_len, prefix_len, partition_size);
+    const CascadeShape c =
+        cascade_shape(pool, num_seqs, num_q_heads, max_context_len, prefix_len, partition_size);
     if (c.suffix_parts > 65535) return PKV_ERR_UNSUPPORTED;
     const WsLayout lay = ws_layout(num_seqs, num_q_heads, pool->head_dim, c.max_parts);
     if (!workspace || !aligned16(workspace) || workspace_bytes < lay.bytes) return PKV_ERR_WORKSPACE;
@@ -478,6 +490,7 @@ pkv_status pkv_paged_attention_decode_cascade(
     pp.prefix_len = prefix_len;
     pp.scale_log2 = scale * 1.4426950408889634f;
     pp.max_parts = c.max_parts;
+    pp.chunks_per_split = c.chunks_per_split;
     pp.ws_m = ws_m;
     pp.ws_l = ws_l;
     pp.ws_o = ws_o;
@@ -508,7 +521,7 @@ pkv_status pkv_paged_attention_decode_cascade(
     p.out_dtype = out_dtype;
     p.direct_single = 0;
     p.skip_tokens = prefix_len;
-    p.part_offset = 1;
+    p.part_offset = c.prefix_splits;
     p.num_queries = 1;
     p.queries_per_cta = 1;
     p.ws_m = ws_m;
@@ -534,7 +547,7 @@ pkv_status pkv_paged_attention_decode_cascade(
     mp.partition_size = c.P;
     mp.skip_single = 0;
     mp.num_queries = 1;
-    mp.prefix_parts = 1;
+    mp.prefix_parts = c.prefix_splits;
     mp.skip_tokens = prefix_len;
     mp.out = out;
     mp.out_dtype = out_dtype;

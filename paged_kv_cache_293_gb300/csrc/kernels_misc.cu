@@ -128,27 +128,97 @@ cudaError_t launch_copy_blocks(const pkv_pool& src, const pkv_pool& dst, const i
 }
 
 // ------------------------------------------------------------------ log-sum-exp merge
-// Row (s, h) with n = prefix_parts + ceil((ctx - skip_tokens) / P) partitions:  M = max_k m_k,
-// out = sum_k e^(m_k - M) o_k / sum_k e^(m_k - M) l_k.  One CTA (4 warps) per row;
-// warp w takes partitions k = w, w + 4, ...; lane j holds dims j, j + 32, ...
-template <int D>
-__global__ void __launch_bounds__(128) lse_merge_kernel(const MergeParams p) {
-    constexpr int NWM = 4, DPL = D / 32;
-    __shared__ float red[NWM][D + 1];
-    __shared__ float smax[NWM];
-    // Launched as a programmatic dependent of the decode kernel: the launch overlaps
-    // the decode's last CTAs, and this waits for the decode grid's results here.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int row = blockIdx.x;
-    const int s = row / (p.num_q_heads * p.num_queries);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+// Row (s, h) with n = prefix_parts + ceil((ctx - skip_tokens) / P) partitions:
+//   M = max_k m_k,  out = sum_k e^(m_k - M) o_k / sum_k e^(m_k - M) l_k.
+// Both kernels are launched as programmatic dependents of the decode kernel: their
+// launch overlaps the decode's last CTAs, and griddepcontrol.wait holds them until the
+// decode grid's partials are complete and visible.
+
+__device__ __forceinline__ int merge_parts(const MergeParams& p, long long row) {
+    const int s = int(row / ((long long)p.num_q_heads * p.num_queries));
     int ctx = p.context_lens[s];
     const long long cap = (long long)p.skip_tokens +
                           (long long)(p.max_parts - p.prefix_parts) * p.partition_size;
     if (ctx < 0) ctx = 0;
     if (ctx > cap) ctx = int(cap);
     const int rest = ctx > p.skip_tokens ? ctx - p.skip_tokens : 0;
-    const int n = p.prefix_parts + (rest + p.partition_size - 1) / p.partition_size;
+    return p.prefix_parts + (rest + p.partition_size - 1) / p.partition_size;
+}
+
+template <int D> struct MergeVec;
+template <> struct MergeVec<128> {
+    static constexpr int N = 4;
+    __device__ __forceinline__ static void load(const float* src, float (&v)[4]) {
+        const float4 x = *reinterpret_cast<const float4*>(src);
+        v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+    }
+};
+template <> struct MergeVec<64> {
+    static constexpr int N = 2;
+    __device__ __forceinline__ static void load(const float* src, float (&v)[2]) {
+        const float2 x = *reinterpret_cast<const float2*>(src);
+        v[0] = x.x; v[1] = x.y;
+    }
+};
+
+// Up to 8 partitions per row: one warp per row, 8 rows per CTA.  Lane k holds
+// partition k's weight; lane j holds dims [j * V, (j + 1) * V) of the sum.
+template <int D>
+__global__ void __launch_bounds__(256) lse_merge_rows_kernel(const MergeParams p, long long rows) {
+    constexpr int V = MergeVec<D>::N;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long row = (long long)blockIdx.x * 8 + warp;
+    if (row >= rows) return;
+    const int n = merge_parts(p, row);
+    if (p.skip_single && n <= 1) return;
+    const float* mrow = p.ws_m + (size_t)row * p.max_parts;
+    const float* lrow = p.ws_l + (size_t)row * p.max_parts;
+    const float* orow = p.ws_o + (size_t)row * p.max_parts * D;
+    float lk = 0.f, mk = -INFINITY;
+    if (lane < n) {
+        lk = lrow[lane];
+        mk = lk > 0.f ? mrow[lane] : -INFINITY;
+    }
+    float M = mk;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL_MASK, M, o));
+    const size_t out_base = (size_t)row * D + lane * V;
+    if (M == -INFINITY) {
+#pragma unroll
+        for (int j = 0; j < V; ++j) store_out(p.out, p.out_dtype, out_base + j, 0.f);
+        return;
+    }
+    const float w = lk > 0.f ? fast_exp2((mk - M) * 1.4426950408889634f) : 0.f;
+    float L = w * lk;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(FULL_MASK, L, o);
+    float acc[V];
+#pragma unroll
+    for (int j = 0; j < V; ++j) acc[j] = 0.f;
+#pragma unroll 8
+    for (int k = 0; k < n; ++k) {
+        const float wk = __shfl_sync(FULL_MASK, w, k);
+        float v[V];
+        MergeVec<D>::load(orow + (size_t)k * D + lane * V, v);
+#pragma unroll
+        for (int j = 0; j < V; ++j) acc[j] = fmaf(wk, v[j], acc[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < V; ++j) store_out(p.out, p.out_dtype, out_base + j, acc[j] / L);
+}
+
+// Many partitions: one CTA of 8 warps per row; warp w takes partitions w, w + 8, ...
+// with several loads in flight, and the warps' sums meet in shared memory.
+template <int D>
+__global__ void __launch_bounds__(256) lse_merge_kernel(const MergeParams p) {
+    constexpr int NWM = 8, V = MergeVec<D>::N;
+    __shared__ float red[NWM][D + 1];
+    __shared__ float smax[NWM];
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const long long row = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n = merge_parts(p, row);
     if (p.skip_single && n <= 1) return;
     const float* mrow = p.ws_m + (size_t)row * p.max_parts;
     const float* lrow = p.ws_l + (size_t)row * p.max_parts;
@@ -161,26 +231,28 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(const MergeParams p) {
     for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL_MASK, M, o));
     if (lane == 0) smax[warp] = M;
     __syncthreads();
-    M = fmaxf(fmaxf(smax[0], smax[1]), fmaxf(smax[2], smax[3]));
+#pragma unroll
+    for (int w = 0; w < NWM; ++w) M = fmaxf(M, smax[w]);
     const size_t out_base = (size_t)row * D;
     if (M == -INFINITY) {
         for (int d = threadIdx.x; d < D; d += NWM * 32) store_out(p.out, p.out_dtype, out_base + d, 0.f);
         return;
     }
-    const float log2e = 1.4426950408889634f;
-    float L = 0.f, O[DPL];
+    float L = 0.f, acc[V];
 #pragma unroll
-    for (int j = 0; j < DPL; ++j) O[j] = 0.f;
+    for (int j = 0; j < V; ++j) acc[j] = 0.f;
 #pragma unroll 4
     for (int k = warp; k < n; k += NWM) {
         const float lk = lrow[k];
-        const float w = lk > 0.f ? fast_exp2((mrow[k] - M) * log2e) : 0.f;
-        L = fmaf(w, lk, L);
+        const float wk = lk > 0.f ? fast_exp2((mrow[k] - M) * 1.4426950408889634f) : 0.f;
+        float v[V];
+        MergeVec<D>::load(orow + (size_t)k * D + lane * V, v);
+        L = fmaf(wk, lk, L);
 #pragma unroll
-        for (int j = 0; j < DPL; ++j) O[j] = fmaf(w, orow[(size_t)k * D + lane + 32 * j], O[j]);
+        for (int j = 0; j < V; ++j) acc[j] = fmaf(wk, v[j], acc[j]);
     }
 #pragma unroll
-    for (int j = 0; j < DPL; ++j) red[warp][lane + 32 * j] = O[j];
+    for (int j = 0; j < V; ++j) red[warp][lane * V + j] = acc[j];
     if (lane == 0) red[warp][D] = L;
     __syncthreads();
     for (int d = threadIdx.x; d < D; d += NWM * 32) {
@@ -192,11 +264,13 @@ __global__ void __launch_bounds__(128) lse_merge_kernel(const MergeParams p) {
 }
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
-    const unsigned rows = (unsigned)((long long)p.num_seqs * p.num_queries * p.num_q_heads);
+    const long long rows = (long long)p.num_seqs * p.num_queries * p.num_q_heads;
     if (rows == 0) return cudaSuccess;
+    if (p.head_dim != 64 && p.head_dim != 128) return cudaErrorInvalidValue;
+    const bool few = p.max_parts <= 8;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(rows);
-    cfg.blockDim = dim3(128);
+    cfg.gridDim = dim3(few ? (unsigned)((rows + 7) / 8) : (unsigned)rows);
+    cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -204,9 +278,11 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (p.head_dim == 64) return cudaLaunchKernelEx(&cfg, lse_merge_kernel<64>, p);
-    if (p.head_dim == 128) return cudaLaunchKernelEx(&cfg, lse_merge_kernel<128>, p);
-    return cudaErrorInvalidValue;
+    if (few)
+        return p.head_dim == 64 ? cudaLaunchKernelEx(&cfg, lse_merge_rows_kernel<64>, p, rows)
+                                : cudaLaunchKernelEx(&cfg, lse_merge_rows_kernel<128>, p, rows);
+    return p.head_dim == 64 ? cudaLaunchKernelEx(&cfg, lse_merge_kernel<64>, p)
+                            : cudaLaunchKernelEx(&cfg, lse_merge_kernel<128>, p);
 }
 
 }  // namespace pkv

@@ -7,8 +7,9 @@
 // physical blocks, their attention over those tokens is one dense contraction per
 // kv head: (num_seqs * G) query rows against prefix_len keys.  This kernel reads
 // the shared pages once per CTA and runs both contractions on mma.sync tensor
-// cores; the per-row result (max score, sum of weights, weighted sum of V) goes
-// to workspace slot 0, beside the partitions of each sequence's own suffix, and
+// cores; the per-row result (max score, sum of weights, weighted sum of V) of
+// each split of the prefix goes to its own workspace slot, before the
+// partitions of each sequence's own suffix, and
 // the log-sum-exp merge combines them -- the same arithmetic as attending to the
 // whole context at once, regrouped.
 //
@@ -39,7 +40,8 @@ struct PrefixParams {
     int32_t max_blocks_per_seq;
     int32_t prefix_len;        // tokens, a multiple of 16 and of the block size
     float scale_log2;
-    int32_t max_parts;         // workspace rows hold max_parts slots; this writes slot 0
+    int32_t max_parts;         // workspace rows hold max_parts slots
+    int32_t chunks_per_split;  // grid.z splits the prefix: split z writes slot z
     float* ws_m;
     float* ws_l;
     float* ws_o;
@@ -85,7 +87,9 @@ prefix_attention_kernel(const __grid_constant__ CUtensorMap tmap_k,
         }
     }
 
-    const int n_chunks = p.prefix_len / CHUNK_TOKENS;
+    // this CTA's share of the prefix: chunks [c0, c0 + n_chunks)
+    const int c0 = blockIdx.z * p.chunks_per_split;
+    const int n_chunks = min(p.prefix_len / CHUNK_TOKENS - c0, p.chunks_per_split);
     const int B = p.block_size;
     const uint64_t policy = l2_evict_first_policy();
     __shared__ int bad_chunk;
@@ -99,7 +103,7 @@ prefix_attention_kernel(const __grid_constant__ CUtensorMap tmap_k,
     auto issue = [&](int c) {  // thread 0 only
         const int st = c % NS;
         const uint32_t bar = bar0 + st * 8;
-        const int t = c * CHUNK_TOKENS;
+        const int t = (c0 + c) * CHUNK_TOKENS;
         const int phys = __ldg(p.block_tables + t / B);
         if ((unsigned)phys >= (unsigned)p.num_blocks) {
             set_error(p.err, PKV_DEVERR_BLOCK_ID);
@@ -117,7 +121,7 @@ prefix_attention_kernel(const __grid_constant__ CUtensorMap tmap_k,
         }
     };
     // every sequence of this tile must hold the same prefix blocks as sequence 0
-    if (kvh == 0) {
+    if (kvh == 0 && blockIdx.z == 0) {
         const int nb = p.prefix_len / B;
         const int s_lo = blockIdx.y * 64 / G;
         const int s_hi = min(p.num_seqs, (blockIdx.y * 64 + 63) / G + 1);
@@ -225,7 +229,7 @@ prefix_attention_kernel(const __grid_constant__ CUtensorMap tmap_k,
     for (int h = 0; h < 2; ++h) {
         const long long qr = h ? qr1 : qr0;
         if (qr < 0) continue;
-        const size_t r = (size_t)qr * p.max_parts;   // slot 0
+        const size_t r = (size_t)qr * p.max_parts + blockIdx.z;
         float* orow = p.ws_o + r * D;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
@@ -251,7 +255,8 @@ cudaError_t launch_prefix_td(const PrefixParams& p, const void* k_pool, const vo
     const int G = p.num_q_heads / p.num_kv_heads;
     const long long tiles = ((long long)p.num_seqs * G + 63) / 64;
     if (tiles > 65535) return cudaErrorNotSupported;
-    dim3 grid(p.num_kv_heads, (unsigned)tiles);
+    const int splits = (p.prefix_len / CHUNK_TOKENS + p.chunks_per_split - 1) / p.chunks_per_split;
+    dim3 grid(p.num_kv_heads, (unsigned)tiles, splits);
     auto kernel = prefix_attention_kernel<T, D>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
