@@ -40,6 +40,7 @@ LENGTH_RECIPES = {
     "llama13b_b32": "lognormal median 512 sigma 1, rounded, clipped [16, 4096]",
     "gqa_prefix": "512 shared + uniform [64, 2048] private",
     "long_splitk": "uniform [32768, 131072]",
+    "system_prompt": "2048 shared + uniform [16, 256] private",
 }
 DEFAULT_WORKLOAD = "llama13b_b16"
 

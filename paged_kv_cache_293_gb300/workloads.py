@@ -232,6 +232,18 @@ def gqa_prefix(seed=0, device="cpu", num_seqs=256):
                  shared_prefix_blocks=32, cow_fraction=0.10)
 
 
+def system_prompt(seed=0, device="cpu", num_seqs=256):
+    """A long shared system prompt with short replies, after the example in "Serving models
+    with vLLM" ("A real example": prefix caching for a 2,000-token system prompt): GQA
+    32 q / 8 kv heads x 128, bf16, B = 16; every sequence = the same 2048-token prefix
+    (128 shared blocks) + a private suffix U[16, 256]."""
+    rng = np.random.default_rng(seed + 6)
+    ctx = 2048 + rng.integers(16, 256, size=num_seqs, endpoint=True)
+    return build("system_prompt_bf16_b16", dtype="bf16", num_q_heads=32, num_kv_heads=8,
+                 head_dim=128, block_size=16, context_lens=ctx, seed=seed, device=device,
+                 shared_prefix_blocks=128)
+
+
 LONG_POOL_BYTES = 20 * 10 ** 9
 
 
@@ -253,6 +265,7 @@ CONFIGS = {
     "llama13b_b32": lambda seed=0, device="cpu", **kw: llama13b(seed, device, 32, **kw),
     "gqa_prefix": gqa_prefix,
     "long_splitk": long_splitk,
+    "system_prompt": system_prompt,
 }
 
 

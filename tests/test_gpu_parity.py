@@ -572,3 +572,18 @@ def test_cascade_flags_a_sequence_with_other_prefix_blocks(P):
     P.pkv_paged_attention_decode_cascade(w.q, w.k_pool, w.v_pool, dev_i32(bt),
                                          dev_i32(w.context_lens), w.scale, out, 100, 32, ws)
     assert P.pkv_get_device_error() & P.DEVERR["PREFIX"]
+
+
+def test_cascade_on_the_system_prompt_batch_matches_oracle(P):
+    """The long-shared-prompt batch through bench.py's cascade step, against the oracle."""
+    import bench
+    w = workloads.make("system_prompt", seed=0, device=DEV, num_seqs=64)
+    st = bench.Step(P, w, torch.device(DEV), fused=True, cascade=True)
+    assert st.prefix_len == 2048
+    st.pre_decode()
+    st.decode()
+    torch.cuda.synchronize()
+    ref = oracle.paged_decode(w.dtype, host(w.k_pool), host(w.v_pool), host(w.q),
+                              w.block_tables, w.context_lens, w.scale)
+    _assert_16bit_close(st.out, ref, w.dtype)
+    assert_no_device_error(P)
