@@ -13,9 +13,11 @@
 // the log-sum-exp merge combines them -- the same arithmetic as attending to the
 // whole context at once, regrouped.
 //
-// CTA: 4 warps x 16 query rows of one kv head.  The prefix's 16-token chunks are
-// staged by TMA tensor copies (128-byte swizzle) into a four-stage ring shared by
-// the four warps.  Per chunk and warp:
+// CTA: 4 compute warps x 16 query rows of one kv head, plus one warp whose lane 0
+// feeds a six-stage ring: the prefix's 16-token chunks are staged by TMA tensor
+// copies (128-byte swizzle) and completed on a per-stage "full" mbarrier; each
+// compute warp releases a stage on its "empty" mbarrier when done with it, so no
+// CTA-wide barrier holds the warps together.  Per chunk and compute warp:
 //   S [16 rows x 16 tokens] = Q [16 x D] . K^T        (2 D/16 MMAs, B = K via ldmatrix)
 //   O [16 rows x D]        += P [16 x 16] . V          (4 D/16 MMAs: P as a 16-bit high
 //                                                       part and remainder, B = V via
@@ -27,7 +29,7 @@
 
 namespace pkv {
 
-constexpr int PREFIX_STAGES = 4;
+constexpr int PREFIX_STAGES = 6;
 
 struct PrefixParams {
     const void* q;             // [S][Hq][D]
@@ -49,25 +51,87 @@ struct PrefixParams {
 };
 
 template <typename T, int D>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(160, 3)
 prefix_attention_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v, const PrefixParams p) {
     using Geo = MmaGeometry<D>;
     constexpr int KS = Geo::KSTEPS, NS = PREFIX_STAGES, NT = D / 8;
+    constexpr int CONSUMERS = 4;  // warps 0-3 compute; warp 4 feeds the ring
     extern __shared__ __align__(128) unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t ring_s = smem_addr(smem);
-    const uint32_t bar0 = smem_addr(smem + NS * Geo::STAGE_BYTES);
+    const uint32_t full0 = smem_addr(smem + NS * Geo::STAGE_BYTES);   // chunk landed
+    const uint32_t empty0 = full0 + NS * 8;                              // chunk released
 
     const int kvh = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g4 = lane >> 2, q4 = lane & 3;
     const int G = p.num_q_heads / p.num_kv_heads;
+    const int B = p.block_size;
+    // this CTA's share of the prefix: chunks [c0, c0 + n_chunks)
+    const int c0 = blockIdx.z * p.chunks_per_split;
+    const int n_chunks = min(p.prefix_len / CHUNK_TOKENS - c0, p.chunks_per_split);
+
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < NS; ++st) {
+            mbar_init(full0 + st * 8, 1);
+            mbar_init(empty0 + st * 8, CONSUMERS);
+        }
+        mbar_init_fence();
+    }
+    // every sequence of this tile must hold the same prefix blocks as sequence 0
+    if (kvh == 0 && blockIdx.z == 0) {
+        const int nb = p.prefix_len / B;
+        const int s_lo = blockIdx.y * 64 / G;
+        const int s_hi = min(p.num_seqs, (blockIdx.y * 64 + 63) / G + 1);
+        for (int i = threadIdx.x; i < (s_hi - s_lo) * nb; i += blockDim.x) {
+            const int s = s_lo + i / nb, j = i % nb;
+            if (p.block_tables[(size_t)s * p.max_blocks_per_seq + j] != p.block_tables[j])
+                set_error(p.err, PKV_DEVERR_PREFIX);
+        }
+    }
+    __syncthreads();
+
+    if (warp == CONSUMERS) {
+        // ---- producer: one lane hands each chunk to the copy engine once its stage is free
+        if (lane != 0) return;
+        const uint64_t policy = l2_evict_first_policy();
+        int issued = 0;
+        for (int c = 0; c < n_chunks; ++c) {
+            const int st = c % NS;
+            if (c >= NS && !mbar_wait(empty0 + st * 8, ((c / NS) - 1) & 1)) {
+                set_error(p.err, PKV_DEVERR_TIMEOUT);
+                break;
+            }
+            const uint32_t bar = full0 + st * 8;
+            const int t = (c0 + c) * CHUNK_TOKENS;
+            const int phys = __ldg(p.block_tables + t / B);
+            if ((unsigned)phys >= (unsigned)p.num_blocks) {
+                set_error(p.err, PKV_DEVERR_BLOCK_ID);
+                mbar_arrive(bar);  // the consumers see a zero-byte phase and skip nothing else
+            } else {
+                const int row = (phys * p.num_kv_heads + kvh) * B + (t % B);
+                const uint32_t dst = ring_s + st * Geo::STAGE_BYTES;
+                mbar_arrive_expect_tx(bar, Geo::STAGE_BYTES);
+#pragma unroll
+                for (int b = 0; b < Geo::BOXES; ++b) {
+                    tma_load_2d(dst + b * Geo::BOX_BYTES, &tmap_k, b * 64, row, bar, policy);
+                    tma_load_2d(dst + Geo::POOL_BYTES + b * Geo::BOX_BYTES, &tmap_v, b * 64, row,
+                                bar, policy);
+                }
+            }
+            issued = c + 1;
+        }
+        // the CTA must not end with copies still landing in its shared memory
+        for (int c = issued > NS ? issued - NS : 0; c < issued; ++c)
+            mbar_wait(full0 + (c % NS) * 8, (c / NS) & 1);
+        return;
+    }
+
+    // ---- consumers: 16 query rows per warp
+    const int g4 = lane >> 2, q4 = lane & 3;
     const int rows = p.num_seqs * G;
     const int row_lo = blockIdx.y * 64 + warp * 16 + g4;  // this lane's rows: row_lo, row_lo + 8
-
-    // q row (s, g) of this kv head, or -1 past the last row
     auto q_row = [&](int r) -> long long {
         return r < rows ? ((long long)(r / G) * p.num_q_heads + kvh * G + r % G) : -1;
     };
@@ -87,68 +151,21 @@ prefix_attention_kernel(const __grid_constant__ CUtensorMap tmap_k,
         }
     }
 
-    // this CTA's share of the prefix: chunks [c0, c0 + n_chunks)
-    const int c0 = blockIdx.z * p.chunks_per_split;
-    const int n_chunks = min(p.prefix_len / CHUNK_TOKENS - c0, p.chunks_per_split);
-    const int B = p.block_size;
-    const uint64_t policy = l2_evict_first_policy();
-    __shared__ int bad_chunk;
-    if (threadIdx.x == 0) {
-        bad_chunk = 0;
-        for (int st = 0; st < NS; ++st) mbar_init(bar0 + st * 8, 1);
-        mbar_init_fence();
-    }
-    __syncthreads();
-
-    auto issue = [&](int c) {  // thread 0 only
-        const int st = c % NS;
-        const uint32_t bar = bar0 + st * 8;
-        const int t = (c0 + c) * CHUNK_TOKENS;
-        const int phys = __ldg(p.block_tables + t / B);
-        if ((unsigned)phys >= (unsigned)p.num_blocks) {
-            set_error(p.err, PKV_DEVERR_BLOCK_ID);
-            bad_chunk = 1;
-            mbar_arrive(bar);
-            return;
-        }
-        const int row = (phys * p.num_kv_heads + kvh) * B + (t % B);
-        const uint32_t dst = ring_s + st * Geo::STAGE_BYTES;
-        mbar_arrive_expect_tx(bar, Geo::STAGE_BYTES);
-#pragma unroll
-        for (int b = 0; b < Geo::BOXES; ++b) {
-            tma_load_2d(dst + b * Geo::BOX_BYTES, &tmap_k, b * 64, row, bar, policy);
-            tma_load_2d(dst + Geo::POOL_BYTES + b * Geo::BOX_BYTES, &tmap_v, b * 64, row, bar, policy);
-        }
-    };
-    // every sequence of this tile must hold the same prefix blocks as sequence 0
-    if (kvh == 0 && blockIdx.z == 0) {
-        const int nb = p.prefix_len / B;
-        const int s_lo = blockIdx.y * 64 / G;
-        const int s_hi = min(p.num_seqs, (blockIdx.y * 64 + 63) / G + 1);
-        for (int i = threadIdx.x; i < (s_hi - s_lo) * nb; i += blockDim.x) {
-            const int s = s_lo + i / nb, j = i % nb;
-            if (p.block_tables[(size_t)s * p.max_blocks_per_seq + j] != p.block_tables[j])
-                set_error(p.err, PKV_DEVERR_PREFIX);
-        }
-    }
-    int issued = 0;  // thread 0's count of chunks handed to the copy engine
-    if (threadIdx.x == 0)
-        for (; issued < NS && issued < n_chunks; ++issued) issue(issued);
-
     float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
     float o[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
     const int mi = lane >> 3, mr = lane & 7;
-    bool timed_out = false;
 
     for (int c = 0; c < n_chunks; ++c) {
         const int st = c % NS;
-        if (!timed_out && !mbar_wait(bar0 + st * 8, (c / NS) & 1)) {
+        if (!__all_sync(FULL_MASK, mbar_wait(full0 + st * 8, (c / NS) & 1))) {
             if (lane == 0) set_error(p.err, PKV_DEVERR_TIMEOUT);
-            timed_out = true;
+            break;
         }
-        if (!timed_out && !bad_chunk) {
+        const int t = (c0 + c) * CHUNK_TOKENS;
+        const bool ok = (unsigned)__ldg(p.block_tables + t / B) < (unsigned)p.num_blocks;
+        if (ok) {
             const uint32_t ks_s = ring_s + st * Geo::STAGE_BYTES;
             const uint32_t vs_s = ks_s + Geo::POOL_BYTES;
             // S = Q . K^T for tokens 0-7 (s0) and 8-15 (s1)
@@ -209,14 +226,8 @@ prefix_attention_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 Mma<T>::run(o[2 * dn + 1], al0, al1, al2, al3, b2, b3);
             }
         }
-        timed_out = __syncthreads_or(timed_out);  // every warp is done with this stage
-        if (timed_out) break;
-        if (threadIdx.x == 0 && issued < n_chunks) issue(issued++);
-    }
-    if (timed_out && threadIdx.x == 0) {
-        // give the copies still in flight a bounded chance to land before the CTA exits
-        for (int c = issued > NS ? issued - NS : 0; c < issued; ++c)
-            mbar_wait(bar0 + (c % NS) * 8, (c / NS) & 1);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + st * 8);  // this warp is done with the stage
     }
 
     // rows' totals over the four lanes of a row
@@ -246,7 +257,7 @@ prefix_attention_kernel(const __grid_constant__ CUtensorMap tmap_k,
 template <typename T, int D>
 cudaError_t launch_prefix_td(const PrefixParams& p, const void* k_pool, const void* v_pool,
                              cudaStream_t stream) {
-    constexpr int SMEM = PREFIX_STAGES * MmaGeometry<D>::STAGE_BYTES + PREFIX_STAGES * 8 + 1024;
+    constexpr int SMEM = PREFIX_STAGES * MmaGeometry<D>::STAGE_BYTES + 2 * PREFIX_STAGES * 8 + 1024;
     CUtensorMap tk, tv;
     const long long rows = (long long)p.num_blocks * p.num_kv_heads * p.block_size;
     if (rows >= (1ll << 31)) return cudaErrorNotSupported;
@@ -267,7 +278,7 @@ cudaError_t launch_prefix_td(const PrefixParams& p, const void* k_pool, const vo
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    kernel<<<grid, 128, SMEM, stream>>>(tk, tv, p);
+    kernel<<<grid, 160, SMEM, stream>>>(tk, tv, p);
     return cudaGetLastError();
 }
 

@@ -587,3 +587,42 @@ def test_cascade_on_the_system_prompt_batch_matches_oracle(P):
                               w.block_tables, w.context_lens, w.scale)
     _assert_16bit_close(st.out, ref, w.dtype)
     assert_no_device_error(P)
+
+
+# ------------------------------------------------------------------ sizes at the edges
+
+@pytest.mark.parametrize("engine", [1, 2], ids=["cuda_cores", "tensor_cores"], indirect=True)
+def test_many_short_ragged_sequences(P, engine):
+    """4096 sequences of 1..80 tokens (a large grid of mostly one-chunk CTAs)."""
+    rng = np.random.default_rng(61)
+    ctx = rng.integers(1, 81, size=4096)
+    w = workloads.build("many", dtype="bf16", num_q_heads=8, num_kv_heads=2, head_dim=64,
+                        block_size=16, context_lens=ctx, seed=61, device=DEV)
+    got = run_decode(P, w, partition_size=0)
+    assert max_abs(got, oracle_decode(w)) <= TOL["bf16"]
+    assert_no_device_error(P)
+
+
+@pytest.mark.parametrize("psize", [0, 64, 1024])
+def test_contexts_that_fill_their_table_rows_exactly(P, psize):
+    """Every context = max_blocks_per_seq * B (no partial last block, no spare table entry),
+    including one exactly one partition long."""
+    B, M = 32, 32
+    w = workloads.build("full", dtype="f16", num_q_heads=16, num_kv_heads=4, head_dim=128,
+                        block_size=B, context_lens=[B * M, B * 2, 1024], seed=62, device=DEV,
+                        table_width=M)
+    assert w.block_tables.shape[1] == M and int(w.context_lens[0]) == B * M
+    got = run_decode(P, w, partition_size=psize)
+    assert max_abs(got, oracle_decode(w)) <= TOL["f16"]
+    assert_no_device_error(P)
+
+
+def test_empty_batch_launches_nothing(P):
+    k = torch.zeros((4, 2, 16, 128), dtype=torch.float16, device=DEV)
+    q = torch.zeros((0, 2, 128), dtype=torch.float16, device=DEV)
+    out = torch.zeros((0, 2, 128), dtype=torch.float32, device=DEV)
+    bt = torch.zeros((0, 1), dtype=torch.int32, device=DEV)
+    ctx = torch.zeros((0,), dtype=torch.int32, device=DEV)
+    P.pkv_paged_attention_decode(q, k, k, bt.reshape(0, 1), ctx, 0.1, out, 0)
+    torch.cuda.synchronize()
+    assert_no_device_error(P)
