@@ -411,23 +411,51 @@ pkv_status pkv_paged_attention_decode_multi(
 namespace {
 
 struct CascadeShape {
-    int32_t P, suffix_parts, prefix_splits, chunks_per_split, max_parts;
+    int32_t P, suffix_parts, prefix_splits, tokens_per_split, max_parts;
 };
 
-// The prefix pass is split along the prefix so that it has about 4 CTAs per SM
-// (152 SMs); each split writes one slot, followed by the suffix partitions.
+// Streaming multiprocessors of the current device (152 when it cannot be asked).
+int32_t sm_count() {
+    static int32_t cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 152;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+// The prefix pass runs one CTA per SM over (kv head, 128-row tile, split of the
+// prefix); the split count minimises waves x (64-token chunks per split + 3), the 3
+// standing for a CTA's fixed cost (query tile, pipeline fill, epilogue).  Each split
+// writes one slot, followed by the suffix partitions.
 CascadeShape cascade_shape(const pkv_pool* pool, int32_t num_seqs, int32_t num_q_heads,
                            int32_t max_ctx, int32_t prefix_len, int32_t partition_size) {
     const int32_t rest = max_ctx > prefix_len ? max_ctx - prefix_len : 0;
     const int32_t P = partition_size > 0 ? partition_size : auto_partition(pool, rest);
     const int32_t sp = rest > 0 ? ceil_div(rest, P) : 1;
     const int32_t G = num_q_heads / pool->num_kv_heads;
-    const int64_t ctas = (int64_t)pool->num_kv_heads * (((int64_t)num_seqs * G + 63) / 64);
-    const int32_t chunks = prefix_len / 16;
-    int32_t splits = (int32_t)std::min<int64_t>(chunks, std::max<int64_t>(1, (608 + ctas - 1) / std::max<int64_t>(ctas, 1)));
-    const int32_t cps = ceil_div(chunks, splits);
-    splits = ceil_div(chunks, cps);
-    return CascadeShape{P, sp, splits, cps, splits + sp};
+    const int64_t ctas = std::max<int64_t>(
+        1, (int64_t)pool->num_kv_heads * (((int64_t)num_seqs * G + 127) / 128));
+    const int64_t sms = sm_count();
+    const int32_t chunks = std::max<int32_t>(1, ceil_div(prefix_len, 64));
+    int32_t best_cps = chunks;
+    int64_t best_cost = INT64_MAX;
+    for (int32_t s = 1; s <= std::min<int32_t>(chunks, 64); ++s) {
+        const int32_t cps = ceil_div(chunks, s);
+        const int64_t splits = ceil_div(chunks, cps);
+        const int64_t waves = (ctas * splits + sms - 1) / sms;
+        const int64_t cost = waves * (cps + 3);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best_cps = cps;
+        }
+    }
+    const int32_t splits = ceil_div(chunks, best_cps);
+    return CascadeShape{P, sp, splits, best_cps * 64, splits + sp};
 }
 
 }  // namespace
@@ -490,7 +518,7 @@ pkv_status pkv_paged_attention_decode_cascade(
     pp.prefix_len = prefix_len;
     pp.scale_log2 = scale * 1.4426950408889634f;
     pp.max_parts = c.max_parts;
-    pp.chunks_per_split = c.chunks_per_split;
+    pp.tokens_per_split = c.tokens_per_split;
     pp.ws_m = ws_m;
     pp.ws_l = ws_l;
     pp.ws_o = ws_o;

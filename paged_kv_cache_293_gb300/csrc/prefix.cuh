@@ -1,35 +1,50 @@
-// prefix.cuh -- attention of every sequence's queries over a prefix all of them share.
+// prefix.cuh -- attention of every sequence's queries over a prefix all of them share,
+// on the fifth-generation tensor cores (tcgen05, accumulators in tensor memory).
 //
 // "Serving models with vLLM", section "How it works: PagedAttention": requests with
 // the same prefix (system prompt, documents) point at the same physical blocks;
 // "What Is vLLM", section "How does PagedAttention work?": prefix sharing.  When
 // every sequence of a batch starts with the same prefix_len tokens in the same
 // physical blocks, their attention over those tokens is one dense contraction per
-// kv head: (num_seqs * G) query rows against prefix_len keys.  This kernel reads
-// the shared pages once per CTA and runs both contractions on mma.sync tensor
-// cores; the per-row result (max score, sum of weights, weighted sum of V) of
-// each split of the prefix goes to its own workspace slot, before the
-// partitions of each sequence's own suffix, and
-// the log-sum-exp merge combines them -- the same arithmetic as attending to the
-// whole context at once, regrouped.
+// kv head: (num_seqs * G) query rows against prefix_len keys.  The per-row result
+// (reference max, sum of weights, weighted sum of V) of each split of the prefix
+// goes to its own workspace slot, before the partitions of each sequence's own
+// suffix, and the log-sum-exp merge combines them -- the same arithmetic as
+// attending to the whole context at once, regrouped.
 //
-// CTA: 4 compute warps x 16 query rows of one kv head, plus one warp whose lane 0
-// feeds a six-stage ring: the prefix's 16-token chunks are staged by TMA tensor
-// copies (128-byte swizzle) and completed on a per-stage "full" mbarrier; each
-// compute warp releases a stage on its "empty" mbarrier when done with it, so no
-// CTA-wide barrier holds the warps together.  Per chunk and compute warp:
-//   S [16 rows x 16 tokens] = Q [16 x D] . K^T        (2 D/16 MMAs, B = K via ldmatrix)
-//   O [16 rows x D]        += P [16 x 16] . V          (4 D/16 MMAs: P as a 16-bit high
-//                                                       part and remainder, B = V via
-//                                                       ldmatrix.trans)
-// with the online softmax of each row in registers (rows g and g + 8 of a lane).
+// CTA = 128 query rows of one kv head (the MMA's M) x one split of the prefix,
+// taken in chunks of 64 tokens.  Ten warps with fixed roles:
+//   warp 8, one lane: TMA tensor copies of each chunk's K and V pages (128-byte
+//     swizzle, 16-token boxes) into a three-stage ring;
+//   warp 9, one lane: issues the MMAs --
+//     S_j [128 rows x 64 tokens] = Q . K_j^T       (tensor memory, two buffers)
+//     O   [128 rows x D]        += P_j . V_j       (tensor memory; P as a 16-bit
+//                                                   high part and its remainder)
+//     and learns of their completion through tcgen05.commit on mbarriers;
+//   warps 0-7: the softmax.  Warp w reads lanes 32 (w % 4) .. + 31 (its rows) and
+//     half w / 4 of each S tile's columns; the two warps of a row quarter agree on
+//     the row's chunk maximum through shared memory.
+// The running maximum is kept lazily: P = 2^(s - m_ref) with the reference m_ref
+// raised only when a chunk's maximum exceeds it by more than 8 (base-2 units), so
+// the O accumulator in tensor memory is rescaled (read, scaled and written back
+// by the row's own threads) only on those chunks.  Every term of a row uses the
+// same m_ref, so the result is the same function of the inputs; P stays below 2^8.
+// Every wait is bounded; a CTA that gives up sets PKV_DEVERR_TIMEOUT and still
+// returns its tensor memory.
 #pragma once
 
+#include <type_traits>
+
 #include "decode_mma.cuh"
+#include "umma.cuh"
 
 namespace pkv {
 
-constexpr int PREFIX_STAGES = 6;
+constexpr int PREFIX_STAGES = 3;
+constexpr int PREFIX_ROWS = 128;     // query rows per CTA
+constexpr int PREFIX_CHUNK = 64;     // prefix tokens per S tile
+constexpr int PREFIX_THREADS = 320;  // 8 softmax warps, a copy warp, an MMA warp
+constexpr float PREFIX_RESCALE_LOG2 = 8.f;
 
 struct PrefixParams {
     const void* q;             // [S][Hq][D]
@@ -43,230 +58,379 @@ struct PrefixParams {
     int32_t prefix_len;        // tokens, a multiple of 16 and of the block size
     float scale_log2;
     int32_t max_parts;         // workspace rows hold max_parts slots
-    int32_t chunks_per_split;  // grid.z splits the prefix: split z writes slot z
+    int32_t tokens_per_split;  // a multiple of 64; grid.z splits the prefix, split z -> slot z
     float* ws_m;
     float* ws_l;
     float* ws_o;
     unsigned int* err;
 };
 
+template <int D>
+struct PrefixSmem {
+    static constexpr int BOXES = D / 64;                        // 128-byte columns of a row
+    static constexpr int Q_BOX = PREFIX_ROWS * 128;             // one 128-byte column of Q
+    static constexpr int KV_BOX = PREFIX_CHUNK * 128;           // one of a chunk of K or V
+    static constexpr int POOL_BYTES = BOXES * KV_BOX;
+    static constexpr int STAGE_BYTES = 2 * POOL_BYTES;          // K then V
+    static constexpr int P_BYTES = PREFIX_ROWS * PREFIX_CHUNK * 2;  // one 16-bit part of P
+    static constexpr int Q_OFF = 0;
+    static constexpr int RING_OFF = Q_OFF + BOXES * Q_BOX;
+    static constexpr int P_OFF = RING_OFF + PREFIX_STAGES * STAGE_BYTES;  // [2][hi, lo]
+    static constexpr int RED_OFF = P_OFF + 4 * P_BYTES;                  // float [2][2][128]
+    static constexpr int BAR_OFF = RED_OFF + 4 * PREFIX_ROWS * 4;
+    static constexpr int NBARS = 2 * PREFIX_STAGES + 8 + 8 + 1;
+    static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBARS * 8;
+    static constexpr int BYTES = TMEM_SLOT_OFF + 16 + 1024;             // + alignment slack
+    static constexpr uint32_t TMEM_COLS = 256;   // S: 2 x 64 columns, O: D columns from 128
+    static constexpr uint32_t O_COL = 2 * PREFIX_CHUNK;
+    static_assert(D == 64 || D == 128, "head_dim");
+    static_assert(BYTES <= 227 * 1024, "shared memory");
+};
+
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 template <typename T, int D>
-__global__ void __launch_bounds__(160, 3)
+__global__ void __launch_bounds__(PREFIX_THREADS, 1)
 prefix_attention_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v, const PrefixParams p) {
-    using Geo = MmaGeometry<D>;
-    constexpr int KS = Geo::KSTEPS, NS = PREFIX_STAGES, NT = D / 8;
-    constexpr int CONSUMERS = 4;  // warps 0-3 compute; warp 4 feeds the ring
+    using L = PrefixSmem<D>;
+    constexpr int NS = PREFIX_STAGES, KS = D / 16;
+    constexpr int COPY_WARP = 8, MMA_WARP = 9;
+    constexpr uint32_t FMT = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
+    constexpr uint32_t IDESC_S = umma::idesc_f16(FMT, false, PREFIX_ROWS, PREFIX_CHUNK);
+    constexpr uint32_t IDESC_O = umma::idesc_f16(FMT, true, PREFIX_ROWS, D);
+
     extern __shared__ __align__(128) unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const uint32_t ring_s = smem_addr(smem);
-    const uint32_t full0 = smem_addr(smem + NS * Geo::STAGE_BYTES);   // chunk landed
-    const uint32_t empty0 = full0 + NS * 8;                              // chunk released
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t q_s = sbase + L::Q_OFF, ring_s = sbase + L::RING_OFF, p_s = sbase + L::P_OFF;
+    float* red = reinterpret_cast<float*>(smem + L::RED_OFF);
+    const uint32_t bar0 = sbase + L::BAR_OFF;
+    // barriers: K/V chunk landed, K/V stage free, S tile ready, S buffer read, P tile
+    // written, P buffer free (its P.V done), row-quarter exchange, all MMAs done
+    auto kv_full = [&](int st) { return bar0 + 8 * st; };
+    auto kv_empty = [&](int st) { return bar0 + 8 * (NS + st); };
+    auto s_full = [&](int b) { return bar0 + 8 * (2 * NS + b); };
+    auto s_free = [&](int b) { return bar0 + 8 * (2 * NS + 2 + b); };
+    auto p_full = [&](int b) { return bar0 + 8 * (2 * NS + 4 + b); };
+    auto p_free = [&](int b) { return bar0 + 8 * (2 * NS + 6 + b); };
+    auto xbar = [&](int qtr, int b) { return bar0 + 8 * (2 * NS + 8 + 2 * qtr + b); };
+    const uint32_t o_done = bar0 + 8 * (2 * NS + 16);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::TMEM_SLOT_OFF);
 
-    const int kvh = blockIdx.x;
+    const int kvh = blockIdx.x, tile = blockIdx.y, split = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.num_q_heads / p.num_kv_heads;
     const int B = p.block_size;
-    // this CTA's share of the prefix: chunks [c0, c0 + n_chunks)
-    const int c0 = blockIdx.z * p.chunks_per_split;
-    const int n_chunks = min(p.prefix_len / CHUNK_TOKENS - c0, p.chunks_per_split);
+    const int rows = p.num_seqs * G;
+    const int t_begin = split * p.tokens_per_split;
+    const int t_end = min(p.prefix_len, t_begin + p.tokens_per_split);
+    const int n_chunks = t_end > t_begin ? (t_end - t_begin + PREFIX_CHUNK - 1) / PREFIX_CHUNK : 0;
 
     if (threadIdx.x == 0) {
         for (int st = 0; st < NS; ++st) {
-            mbar_init(full0 + st * 8, 1);
-            mbar_init(empty0 + st * 8, CONSUMERS);
+            mbar_init(kv_full(st), 1);
+            mbar_init(kv_empty(st), 1);
         }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(s_full(b), 1);
+            mbar_init(s_free(b), 8);
+            mbar_init(p_full(b), 8);
+            mbar_init(p_free(b), 1);
+            for (int qtr = 0; qtr < 4; ++qtr) mbar_init(xbar(qtr, b), 2);
+        }
+        mbar_init(o_done, 1);
         mbar_init_fence();
     }
+    if (warp == MMA_WARP) umma::alloc(smem_addr(tmem_slot), L::TMEM_COLS);
+
     // every sequence of this tile must hold the same prefix blocks as sequence 0
-    if (kvh == 0 && blockIdx.z == 0) {
+    if (kvh == 0 && split == 0) {
         const int nb = p.prefix_len / B;
-        const int s_lo = blockIdx.y * 64 / G;
-        const int s_hi = min(p.num_seqs, (blockIdx.y * 64 + 63) / G + 1);
+        const int s_lo = tile * PREFIX_ROWS / G;
+        const int s_hi = min(p.num_seqs, (tile * PREFIX_ROWS + PREFIX_ROWS - 1) / G + 1);
         for (int i = threadIdx.x; i < (s_hi - s_lo) * nb; i += blockDim.x) {
             const int s = s_lo + i / nb, j = i % nb;
             if (p.block_tables[(size_t)s * p.max_blocks_per_seq + j] != p.block_tables[j])
                 set_error(p.err, PKV_DEVERR_PREFIX);
         }
     }
+    // Q tile -> shared memory as the first MMA's A operand (rows past the batch are zero)
+    if (warp < 8) {
+        const int i = threadIdx.x & (PREFIX_ROWS - 1), h = threadIdx.x >> 7;
+        const int r = tile * PREFIX_ROWS + i;
+        const long long qr =
+            r < rows ? (long long)(r / G) * p.num_q_heads + (long long)kvh * G + r % G : -1;
+        const uint4* src =
+            reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + (qr < 0 ? 0 : qr) * D);
+        constexpr int HALF = D / 16;  // 16-byte columns per half row
+#pragma unroll
+        for (int c = h * HALF; c < (h + 1) * HALF; ++c) {
+            const uint4 v = qr >= 0 ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(smem + L::Q_OFF + (c / 8) * L::Q_BOX + swz(i, c % 8)) = v;
+        }
+        umma::fence_smem_to_async();
+    }
+    umma::fence_before_sync();
     __syncthreads();
+    umma::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
 
-    if (warp == CONSUMERS) {
-        // ---- producer: one lane hands each chunk to the copy engine once its stage is free
-        if (lane != 0) return;
-        const uint64_t policy = l2_evict_first_policy();
-        int issued = 0;
-        for (int c = 0; c < n_chunks; ++c) {
-            const int st = c % NS;
-            if (c >= NS && !mbar_wait(empty0 + st * 8, ((c / NS) - 1) & 1)) {
-                set_error(p.err, PKV_DEVERR_TIMEOUT);
-                break;
-            }
-            const uint32_t bar = full0 + st * 8;
-            const int t = (c0 + c) * CHUNK_TOKENS;
-            const int phys = __ldg(p.block_tables + t / B);
-            if ((unsigned)phys >= (unsigned)p.num_blocks) {
-                set_error(p.err, PKV_DEVERR_BLOCK_ID);
-                mbar_arrive(bar);  // the consumers see a zero-byte phase and skip nothing else
-            } else {
-                const int row = (phys * p.num_kv_heads + kvh) * B + (t % B);
-                const uint32_t dst = ring_s + st * Geo::STAGE_BYTES;
-                mbar_arrive_expect_tx(bar, Geo::STAGE_BYTES);
-#pragma unroll
-                for (int b = 0; b < Geo::BOXES; ++b) {
-                    tma_load_2d(dst + b * Geo::BOX_BYTES, &tmap_k, b * 64, row, bar, policy);
-                    tma_load_2d(dst + Geo::POOL_BYTES + b * Geo::BOX_BYTES, &tmap_v, b * 64, row,
-                                bar, policy);
+    if (warp == COPY_WARP) {
+        // ---- copies: each chunk's pages, once its stage has been released
+        if (lane == 0) {
+            const uint64_t policy = l2_evict_last_policy();  // every tile of the head re-reads them
+            int issued = 0;
+            for (int j = 0; j < n_chunks; ++j) {
+                const int st = j % NS;
+                if (j >= NS && !mbar_wait(kv_empty(st), ((j / NS) - 1) & 1)) {
+                    set_error(p.err, PKV_DEVERR_TIMEOUT);
+                    break;
                 }
+                const int t0 = t_begin + j * PREFIX_CHUNK;
+                const int boxes = min(PREFIX_CHUNK, t_end - t0) / CHUNK_TOKENS;
+                int row[PREFIX_CHUNK / CHUNK_TOKENS];
+                int good = 0;
+#pragma unroll
+                for (int b = 0; b < PREFIX_CHUNK / CHUNK_TOKENS; ++b) {
+                    row[b] = -1;
+                    if (b >= boxes) continue;
+                    const int t = t0 + b * CHUNK_TOKENS;
+                    const int phys = __ldg(p.block_tables + t / B);
+                    if ((unsigned)phys >= (unsigned)p.num_blocks) {
+                        set_error(p.err, PKV_DEVERR_BLOCK_ID);  // that piece is not loaded
+                    } else {
+                        row[b] = (phys * p.num_kv_heads + kvh) * B + (t % B);
+                        ++good;
+                    }
+                }
+                const uint32_t bar = kv_full(st);
+                mbar_arrive_expect_tx(bar, (uint32_t)good * 2 * L::BOXES * CHUNK_TOKENS * 128);
+                const uint32_t dst = ring_s + st * L::STAGE_BYTES;
+#pragma unroll
+                for (int b = 0; b < PREFIX_CHUNK / CHUNK_TOKENS; ++b) {
+                    if (row[b] < 0) continue;
+#pragma unroll
+                    for (int x = 0; x < L::BOXES; ++x) {
+                        const uint32_t off = x * L::KV_BOX + b * CHUNK_TOKENS * 128;
+                        tma_load_2d(dst + off, &tmap_k, x * 64, row[b], bar, policy);
+                        tma_load_2d(dst + L::POOL_BYTES + off, &tmap_v, x * 64, row[b], bar, policy);
+                    }
+                }
+                issued = j + 1;
             }
-            issued = c + 1;
-        }
-        // the CTA must not end with copies still landing in its shared memory
-        for (int c = issued > NS ? issued - NS : 0; c < issued; ++c)
-            mbar_wait(full0 + (c % NS) * 8, (c / NS) & 1);
-        return;
-    }
-
-    // ---- consumers: 16 query rows per warp
-    const int g4 = lane >> 2, q4 = lane & 3;
-    const int rows = p.num_seqs * G;
-    const int row_lo = blockIdx.y * 64 + warp * 16 + g4;  // this lane's rows: row_lo, row_lo + 8
-    auto q_row = [&](int r) -> long long {
-        return r < rows ? ((long long)(r / G) * p.num_q_heads + kvh * G + r % G) : -1;
-    };
-    const long long qr0 = q_row(row_lo), qr1 = q_row(row_lo + 8);
-
-    // Q as mma A fragments (rows g4 / g4 + 8, dims of k-step ks)
-    uint32_t qa[KS][4];
-    {
-        const T* q = static_cast<const T*>(p.q);
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            const int d = ks * 16 + 2 * q4;
-            qa[ks][0] = qr0 >= 0 ? __ldg(reinterpret_cast<const uint32_t*>(q + qr0 * D + d)) : 0u;
-            qa[ks][1] = qr1 >= 0 ? __ldg(reinterpret_cast<const uint32_t*>(q + qr1 * D + d)) : 0u;
-            qa[ks][2] = qr0 >= 0 ? __ldg(reinterpret_cast<const uint32_t*>(q + qr0 * D + d + 8)) : 0u;
-            qa[ks][3] = qr1 >= 0 ? __ldg(reinterpret_cast<const uint32_t*>(q + qr1 * D + d + 8)) : 0u;
-        }
-    }
-
-    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-    float o[NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-    const int mi = lane >> 3, mr = lane & 7;
-
-    for (int c = 0; c < n_chunks; ++c) {
-        const int st = c % NS;
-        if (!__all_sync(FULL_MASK, mbar_wait(full0 + st * 8, (c / NS) & 1))) {
-            if (lane == 0) set_error(p.err, PKV_DEVERR_TIMEOUT);
-            break;
-        }
-        const int t = (c0 + c) * CHUNK_TOKENS;
-        const bool ok = (unsigned)__ldg(p.block_tables + t / B) < (unsigned)p.num_blocks;
-        if (ok) {
-            const uint32_t ks_s = ring_s + st * Geo::STAGE_BYTES;
-            const uint32_t vs_s = ks_s + Geo::POOL_BYTES;
-            // S = Q . K^T for tokens 0-7 (s0) and 8-15 (s1)
-            float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                const int row = ((mi >> 1) << 3) + mr;       // token
-                const int col = 2 * ks + (mi & 1);            // 16-byte column of dims
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(ks_s + (col / 8) * Geo::BOX_BYTES + swz(row, col & 7), b0, b1, b2, b3);
-                Mma<T>::run(s0, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-                Mma<T>::run(s1, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
-            }
-            // online softmax: row g4 holds s0[0..1], s1[0..1]; row g4 + 8 holds [2..3]
-            float pr0[4], pr1[4], alpha[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const float a = s0[2 * h] * p.scale_log2, b = s0[2 * h + 1] * p.scale_log2;
-                const float c_ = s1[2 * h] * p.scale_log2, d_ = s1[2 * h + 1] * p.scale_log2;
-                float bm = fmaxf(fmaxf(a, b), fmaxf(c_, d_));
-                bm = fmaxf(bm, __shfl_xor_sync(FULL_MASK, bm, 1));
-                bm = fmaxf(bm, __shfl_xor_sync(FULL_MASK, bm, 2));
-                const float mn = fmaxf(m[h], bm);
-                alpha[h] = fast_exp2(m[h] - mn);
-                m[h] = mn;
-                pr0[2 * h] = fast_exp2(a - mn);
-                pr0[2 * h + 1] = fast_exp2(b - mn);
-                pr1[2 * h] = fast_exp2(c_ - mn);
-                pr1[2 * h + 1] = fast_exp2(d_ - mn);
-                l[h] = l[h] * alpha[h] + pr0[2 * h] + pr0[2 * h + 1] + pr1[2 * h] + pr1[2 * h + 1];
-            }
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                o[nt][0] *= alpha[0]; o[nt][1] *= alpha[0];
-                o[nt][2] *= alpha[1]; o[nt][3] *= alpha[1];
-            }
-            // P as A fragments: a0 row g4 tokens 2q4.., a1 row g4+8, a2/a3 the same for tokens 8..
-            const uint32_t ah0 = Mma<T>::pack(pr0[0], pr0[1]), ah1 = Mma<T>::pack(pr0[2], pr0[3]);
-            const uint32_t ah2 = Mma<T>::pack(pr1[0], pr1[1]), ah3 = Mma<T>::pack(pr1[2], pr1[3]);
-            const uint32_t al0 = Mma<T>::pack(pr0[0] - Mma<T>::round_trip(pr0[0]),
-                                              pr0[1] - Mma<T>::round_trip(pr0[1]));
-            const uint32_t al1 = Mma<T>::pack(pr0[2] - Mma<T>::round_trip(pr0[2]),
-                                              pr0[3] - Mma<T>::round_trip(pr0[3]));
-            const uint32_t al2 = Mma<T>::pack(pr1[0] - Mma<T>::round_trip(pr1[0]),
-                                              pr1[1] - Mma<T>::round_trip(pr1[1]));
-            const uint32_t al3 = Mma<T>::pack(pr1[2] - Mma<T>::round_trip(pr1[2]),
-                                              pr1[3] - Mma<T>::round_trip(pr1[3]));
-            // O += P . V, two 8-dim column tiles per ldmatrix.x4.trans
-#pragma unroll
-            for (int dn = 0; dn < D / 16; ++dn) {
-                const int row = ((mi & 1) << 3) + mr;         // token
-                const int col = 2 * dn + (mi >> 1);            // 16-byte column of dims
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_trans(vs_s + (col / 8) * Geo::BOX_BYTES + swz(row, col & 7), b0, b1, b2, b3);
-                Mma<T>::run(o[2 * dn], ah0, ah1, ah2, ah3, b0, b1);
-                Mma<T>::run(o[2 * dn], al0, al1, al2, al3, b0, b1);
-                Mma<T>::run(o[2 * dn + 1], ah0, ah1, ah2, ah3, b2, b3);
-                Mma<T>::run(o[2 * dn + 1], al0, al1, al2, al3, b2, b3);
-            }
+            // the CTA must not end with copies still landing in its shared memory
+            for (int j = issued > NS ? issued - NS : 0; j < issued; ++j)
+                mbar_wait(kv_full(j % NS), (j / NS) & 1);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(empty0 + st * 8);  // this warp is done with the stage
+    } else if (warp == MMA_WARP) {
+        // ---- MMA issue: S_j as soon as K_j is in, then the P.V of chunk j - 1
+        if (lane == 0) {
+            auto issue_pv = [&](int i) -> bool {
+                if (!mbar_wait(p_full(i & 1), (i >> 1) & 1)) return false;
+                umma::fence_after_sync();
+                const int vt = min(PREFIX_CHUNK, t_end - (t_begin + i * PREFIX_CHUNK));
+                const uint32_t v_s = ring_s + (i % NS) * L::STAGE_BYTES + L::POOL_BYTES;
+                const uint32_t ph = p_s + (i & 1) * 2 * L::P_BYTES, pl = ph + L::P_BYTES;
+                for (int kk = 0; kk < vt / 16; ++kk) {
+                    // V is N-major: 64-dim blocks KV_BOX apart, 8-token groups 1024 apart
+                    const uint64_t bv = umma::sw128_desc(v_s + kk * 16 * 128, L::KV_BOX, 1024);
+                    umma::mma_f16(tmem + L::O_COL, umma::sw128_desc(ph + kk * 32, 16, 1024), bv,
+                                  IDESC_O, (i > 0 || kk > 0) ? 1u : 0u);
+                    umma::mma_f16(tmem + L::O_COL, umma::sw128_desc(pl + kk * 32, 16, 1024), bv,
+                                  IDESC_O, 1u);
+                }
+                umma::commit(p_free(i & 1));
+                umma::commit(kv_empty(i % NS));
+                return true;
+            };
+            bool ok = true;
+            for (int j = 0; j < n_chunks && ok; ++j) {
+                const int st = j % NS;
+                ok = mbar_wait(kv_full(st), (j / NS) & 1) &&
+                     (j < 2 || mbar_wait(s_free(j & 1), ((j - 2) >> 1) & 1));
+                if (!ok) break;
+                umma::fence_after_sync();
+                const uint32_t k_s = ring_s + st * L::STAGE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < KS; ++kk) {
+                    const uint64_t a =
+                        umma::sw128_desc(q_s + (kk >> 2) * L::Q_BOX + (kk & 3) * 32, 16, 1024);
+                    const uint64_t b =
+                        umma::sw128_desc(k_s + (kk >> 2) * L::KV_BOX + (kk & 3) * 32, 16, 1024);
+                    umma::mma_f16(tmem + (j & 1) * PREFIX_CHUNK, a, b, IDESC_S, kk > 0 ? 1u : 0u);
+                }
+                umma::commit(s_full(j & 1));
+                if (j >= 1) ok = issue_pv(j - 1);
+            }
+            if (ok && n_chunks > 0) ok = issue_pv(n_chunks - 1);
+            if (!ok) set_error(p.err, PKV_DEVERR_TIMEOUT);
+            umma::commit(o_done);  // arrives once every MMA above has completed
+            if (!mbar_wait(o_done, 0)) set_error(p.err, PKV_DEVERR_TIMEOUT);
+        }
+        __syncwarp();
+    } else {
+        // ---- softmax: this thread's row i, columns of half h of each S tile
+        const int qtr = warp & 3, h = warp >> 2;
+        const int i = qtr * 32 + lane;
+        const uint32_t lane_tmem = tmem + ((uint32_t)(qtr * 32) << 16);
+        unsigned char* p_g = smem + L::P_OFF;
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        // the two warps of a row quarter swap one float per row through shared memory
+        auto exchange = [&](int j, float v) -> float {
+            red[((j & 1) * 2 + h) * PREFIX_ROWS + i] = v;
+            __threadfence_block();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(xbar(qtr, j & 1));
+            if (!__all_sync(FULL_MASK, mbar_wait(xbar(qtr, j & 1), (j >> 1) & 1))) {
+                ok = false;
+                return v;
+            }
+            return red[((j & 1) * 2 + (h ^ 1)) * PREFIX_ROWS + i];
+        };
+        for (int j = 0; j < n_chunks; ++j) {
+            const int vt = min(PREFIX_CHUNK, t_end - (t_begin + j * PREFIX_CHUNK));
+            if (!__all_sync(FULL_MASK, mbar_wait(s_full(j & 1), (j >> 1) & 1))) {
+                ok = false;
+                break;
+            }
+            umma::fence_after_sync();
+            float s[32];
+            umma::ld32(lane_tmem + (j & 1) * PREFIX_CHUNK + h * 32, s);
+            umma::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_free(j & 1));
+            // columns past the chunk's last token hold no key: they take no part
+            const int nvalid = vt - h * 32;
+            float cm = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                s[k] *= p.scale_log2;
+                if (k < nvalid) cm = fmaxf(cm, s[k]);
+            }
+            cm = fmaxf(cm, exchange(j, cm));
+            if (!ok) break;
+            const bool need = cm > m_ref + PREFIX_RESCALE_LOG2;
+            float alpha = 1.f;
+            if (need) {
+                alpha = fast_exp2(m_ref - cm);
+                m_ref = cm;
+                l *= alpha;
+            }
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                s[k] = k < nvalid ? fast_exp2(s[k] - m_ref) : 0.f;
+                l += s[k];
+            }
+            // the P buffer is free once the P.V of chunk j - 2 is done
+            if (j >= 2 && !__all_sync(FULL_MASK, mbar_wait(p_free(j & 1), ((j - 2) >> 1) & 1))) {
+                ok = false;
+                break;
+            }
+            unsigned char* ph = p_g + (j & 1) * 2 * L::P_BYTES;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {  // 8 tokens per 16-byte column
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float a = s[cc * 8 + 2 * e], b = s[cc * 8 + 2 * e + 1];
+                    hi[e] = Mma<T>::pack(a, b);
+                    lo[e] = Mma<T>::pack(a - Mma<T>::round_trip(a), b - Mma<T>::round_trip(b));
+                }
+                const uint32_t off = swz(i, h * 4 + cc);
+                *reinterpret_cast<uint4*>(ph + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(ph + L::P_BYTES + off) =
+                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+            umma::fence_smem_to_async();
+            // rows whose reference rose: scale their O (complete through chunk j - 1)
+            if (j >= 1 && __any_sync(FULL_MASK, need)) {
+                if (!__all_sync(FULL_MASK, mbar_wait(p_free((j - 1) & 1), ((j - 1) >> 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                umma::fence_after_sync();
+#pragma unroll
+                for (int c = 0; c < D / 2; c += 32) {
+                    float o[32];
+                    umma::ld32(lane_tmem + L::O_COL + h * (D / 2) + c, o);
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) o[k] *= alpha;
+                    umma::st32(lane_tmem + L::O_COL + h * (D / 2) + c, o);
+                }
+                umma::wait_st();
+            }
+            umma::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full(j & 1));
+        }
+        if (ok && n_chunks > 0) {
+            ok = __all_sync(FULL_MASK, mbar_wait(o_done, 0));
+            if (ok) l += exchange(n_chunks, l);
+        }
+        const int r = tile * PREFIX_ROWS + i;
+        const long long qr =
+            r < rows ? (long long)(r / G) * p.num_q_heads + (long long)kvh * G + r % G : -1;
+        const size_t slot = (size_t)(qr < 0 ? 0 : qr) * p.max_parts + split;
+        float* orow = p.ws_o + slot * D + h * (D / 2);
+        if (ok) {
+            umma::fence_after_sync();
+#pragma unroll
+            for (int c = 0; c < D / 2; c += 32) {
+                float o[32];
+                if (n_chunks > 0) {
+                    umma::ld32(lane_tmem + L::O_COL + h * (D / 2) + c, o);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) o[k] = 0.f;
+                }
+                if (qr >= 0) {
+#pragma unroll
+                    for (int k = 0; k < 32; k += 4)
+                        *reinterpret_cast<float4*>(orow + c + k) =
+                            make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
+                }
+            }
+            if (qr >= 0 && h == 0) {
+                p.ws_m[slot] = m_ref * 0.69314718055994530942f;  // natural-log units
+                p.ws_l[slot] = l;
+            }
+        } else if (lane == 0) {
+            set_error(p.err, PKV_DEVERR_TIMEOUT);
+        }
     }
 
-    // rows' totals over the four lanes of a row
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        l[h] += __shfl_xor_sync(FULL_MASK, l[h], 1);
-        l[h] += __shfl_xor_sync(FULL_MASK, l[h], 2);
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const long long qr = h ? qr1 : qr0;
-        if (qr < 0) continue;
-        const size_t r = (size_t)qr * p.max_parts + blockIdx.z;
-        float* orow = p.ws_o + r * D;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            orow[nt * 8 + 2 * q4] = o[nt][2 * h];
-            orow[nt * 8 + 2 * q4 + 1] = o[nt][2 * h + 1];
-        }
-        if (q4 == 0) {
-            p.ws_m[r] = m[h] * 0.69314718055994530942f;  // natural-log units
-            p.ws_l[r] = l[h];
-        }
+    // tensor memory goes back only after every warp is done with it
+    umma::fence_before_sync();
+    __syncthreads();
+    if (warp == MMA_WARP) {
+        umma::fence_after_sync();
+        umma::dealloc(tmem, L::TMEM_COLS);
     }
 }
 
 template <typename T, int D>
 cudaError_t launch_prefix_td(const PrefixParams& p, const void* k_pool, const void* v_pool,
                              cudaStream_t stream) {
-    constexpr int SMEM = PREFIX_STAGES * MmaGeometry<D>::STAGE_BYTES + 2 * PREFIX_STAGES * 8 + 1024;
+    constexpr int SMEM = PrefixSmem<D>::BYTES;
+    if (p.tokens_per_split <= 0 || p.tokens_per_split % PREFIX_CHUNK != 0)
+        return cudaErrorInvalidValue;
     CUtensorMap tk, tv;
     const long long rows = (long long)p.num_blocks * p.num_kv_heads * p.block_size;
     if (rows >= (1ll << 31)) return cudaErrorNotSupported;
     if (!encode_pool_map<T>(&tk, k_pool, rows, D) || !encode_pool_map<T>(&tv, v_pool, rows, D))
         return cudaErrorNotSupported;
     const int G = p.num_q_heads / p.num_kv_heads;
-    const long long tiles = ((long long)p.num_seqs * G + 63) / 64;
+    const long long tiles = ((long long)p.num_seqs * G + PREFIX_ROWS - 1) / PREFIX_ROWS;
     if (tiles > 65535) return cudaErrorNotSupported;
-    const int splits = (p.prefix_len / CHUNK_TOKENS + p.chunks_per_split - 1) / p.chunks_per_split;
+    const int splits = (p.prefix_len + p.tokens_per_split - 1) / p.tokens_per_split;
     dim3 grid(p.num_kv_heads, (unsigned)tiles, splits);
     auto kernel = prefix_attention_kernel<T, D>;
     int dev = 0;
@@ -278,7 +442,7 @@ cudaError_t launch_prefix_td(const PrefixParams& p, const void* k_pool, const vo
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    kernel<<<grid, 160, SMEM, stream>>>(tk, tv, p);
+    kernel<<<grid, PREFIX_THREADS, SMEM, stream>>>(tk, tv, p);
     return cudaGetLastError();
 }
 

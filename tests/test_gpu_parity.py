@@ -574,6 +574,36 @@ def test_cascade_flags_a_sequence_with_other_prefix_blocks(P):
     assert P.pkv_get_device_error() & P.DEVERR["PREFIX"]
 
 
+def test_cascade_prefix_pass_rescales_when_scores_grow(P):
+    """Keys scaled by 1 + 15 t / 640 along a 640-token shared prefix: each row's
+    maximum keeps rising, so the prefix pass raises its reference maximum and
+    rescales the accumulated O on later chunks (250 sequences x G = 4: eight tiles,
+    the last partial, and splits of three 64-token chunks)."""
+    B, nb = 16, 40
+    ctx = [nb * B + x for x in (3, 17, 64, 200, 1)] * 50
+    w = workloads.build("cascade_grow", dtype="bf16", num_q_heads=16, num_kv_heads=4,
+                        head_dim=128, block_size=B, context_lens=ctx, seed=54, device=DEV,
+                        shared_prefix_blocks=nb)
+    blocks = torch.as_tensor(w.block_tables[0, :nb].astype(np.int64), device=DEV)
+    t = torch.arange(nb * B, device=DEV, dtype=torch.float32)
+    w.k_pool[blocks] = (w.k_pool[blocks].float() * (1 + 15 * t / (nb * B)).view(nb, 1, B, 1)).to(
+        w.k_pool.dtype)
+    Lp, mcl = nb * B, w.max_context_len
+    ws = P.workspace_tensor(P.pkv_cascade_workspace_bytes(w.k_pool, w.num_seqs, 16, mcl, Lp), DEV)
+    out = torch.full((w.num_seqs, 16, 128), float("nan"), dtype=torch.float32, device=DEV)
+    P.pkv_paged_attention_decode_cascade(w.q, w.k_pool, w.v_pool, dev_i32(w.block_tables),
+                                         dev_i32(w.context_lens), w.scale, out, mcl, Lp, ws)
+    torch.cuda.synchronize()
+    ref = oracle.paged_decode("bf16", host(w.k_pool), host(w.v_pool), host(w.q), w.block_tables,
+                              w.context_lens, w.scale)
+    assert max_abs(out, ref) <= TOL["bf16"]
+    # both paths carry each weight as a 16-bit pair (relative error <= 2^-18) against
+    # V rows of magnitude up to about 4, on attention concentrated on a few tokens
+    plain = run_decode(P, w)
+    assert max_abs(out, plain.double().cpu().numpy()) <= 5e-5
+    assert_no_device_error(P)
+
+
 def test_cascade_on_the_system_prompt_batch_matches_oracle(P):
     """The long-shared-prompt batch through bench.py's cascade step, against the oracle."""
     import bench
