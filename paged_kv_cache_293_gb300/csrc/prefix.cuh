@@ -13,13 +13,16 @@
 // attending to the whole context at once, regrouped.
 //
 // CTA = 128 query rows of one kv head (the MMA's M) x one split of the prefix,
-// taken in chunks of 64 tokens.  Ten warps with fixed roles:
-//   warp 8, one lane: TMA tensor copies of each chunk's K and V pages (128-byte
-//     swizzle, 16-token boxes) into a three-stage ring;
+// taken in chunks of 64 tokens.  Eleven warps with fixed roles:
+//   warps 8 and 10, one lane each: TMA tensor copies of each chunk's K pages
+//     (warp 8) and V pages (warp 10) -- 128-byte swizzle, 16-token boxes -- into a
+//     six-stage K ring and a five-stage V ring; a K stage is released as soon as
+//     its Q.K^T is done, a V stage after its P.V;
 //   warp 9, one lane: issues the MMAs --
-//     S_j [128 rows x 64 tokens] = Q . K_j^T       (tensor memory, two buffers)
-//     O   [128 rows x D]        += P_j . V_j       (tensor memory; P as a 16-bit
-//                                                   high part and its remainder)
+//     S_j [128 rows x 64 tokens] = Q . K_j^T   (tensor memory, two buffers)
+//     O   [128 rows x D]        += P_j . V_j   (tensor memory; P_j is written over
+//                                               S_j as a 16-bit high part and its
+//                                               remainder and read from there)
 //     and learns of their completion through tcgen05.commit on mbarriers;
 //   warps 0-7: the softmax.  Warp w reads lanes 32 (w % 4) .. + 31 (its rows) and
 //     half w / 4 of each S tile's columns; the two warps of a row quarter agree on
@@ -40,10 +43,11 @@
 
 namespace pkv {
 
-constexpr int PREFIX_STAGES = 3;
+constexpr int PREFIX_K_STAGES = 6;
+constexpr int PREFIX_V_STAGES = 5;
 constexpr int PREFIX_ROWS = 128;     // query rows per CTA
 constexpr int PREFIX_CHUNK = 64;     // prefix tokens per S tile
-constexpr int PREFIX_THREADS = 320;  // 8 softmax warps, a copy warp, an MMA warp
+constexpr int PREFIX_THREADS = 352;  // 8 softmax warps, K copies, MMA issue, V copies
 constexpr float PREFIX_RESCALE_LOG2 = 8.f;
 
 struct PrefixParams {
@@ -70,18 +74,17 @@ struct PrefixSmem {
     static constexpr int BOXES = D / 64;                        // 128-byte columns of a row
     static constexpr int Q_BOX = PREFIX_ROWS * 128;             // one 128-byte column of Q
     static constexpr int KV_BOX = PREFIX_CHUNK * 128;           // one of a chunk of K or V
-    static constexpr int POOL_BYTES = BOXES * KV_BOX;
-    static constexpr int STAGE_BYTES = 2 * POOL_BYTES;          // K then V
-    static constexpr int P_BYTES = PREFIX_ROWS * PREFIX_CHUNK * 2;  // one 16-bit part of P
+    static constexpr int STAGE_BYTES = BOXES * KV_BOX;          // a chunk of one pool
     static constexpr int Q_OFF = 0;
-    static constexpr int RING_OFF = Q_OFF + BOXES * Q_BOX;
-    static constexpr int P_OFF = RING_OFF + PREFIX_STAGES * STAGE_BYTES;  // [2][hi, lo]
-    static constexpr int RED_OFF = P_OFF + 4 * P_BYTES;                  // float [2][2][128]
+    static constexpr int K_OFF = Q_OFF + BOXES * Q_BOX;
+    static constexpr int V_OFF = K_OFF + PREFIX_K_STAGES * STAGE_BYTES;
+    static constexpr int RED_OFF = V_OFF + PREFIX_V_STAGES * STAGE_BYTES;  // float [2][2][128]
     static constexpr int BAR_OFF = RED_OFF + 4 * PREFIX_ROWS * 4;
-    static constexpr int NBARS = 2 * PREFIX_STAGES + 8 + 8 + 1;
+    static constexpr int NBARS = 2 * PREFIX_K_STAGES + 2 * PREFIX_V_STAGES + 6 + 8 + 2;
     static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBARS * 8;
     static constexpr int BYTES = TMEM_SLOT_OFF + 16 + 1024;             // + alignment slack
-    static constexpr uint32_t TMEM_COLS = 256;   // S: 2 x 64 columns, O: D columns from 128
+    // tensor memory: S_j / P_j in columns 64 (j % 2) .. + 63, O from column 128
+    static constexpr uint32_t TMEM_COLS = 256;
     static constexpr uint32_t O_COL = 2 * PREFIX_CHUNK;
     static_assert(D == 64 || D == 128, "head_dim");
     static_assert(BYTES <= 227 * 1024, "shared memory");
@@ -98,8 +101,8 @@ __global__ void __launch_bounds__(PREFIX_THREADS, 1)
 prefix_attention_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v, const PrefixParams p) {
     using L = PrefixSmem<D>;
-    constexpr int NS = PREFIX_STAGES, KS = D / 16;
-    constexpr int COPY_WARP = 8, MMA_WARP = 9;
+    constexpr int NK = PREFIX_K_STAGES, NV = PREFIX_V_STAGES, KS = D / 16;
+    constexpr int K_WARP = 8, MMA_WARP = 9, V_WARP = 10;
     constexpr uint32_t FMT = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
     constexpr uint32_t IDESC_S = umma::idesc_f16(FMT, false, PREFIX_ROWS, PREFIX_CHUNK);
     constexpr uint32_t IDESC_O = umma::idesc_f16(FMT, true, PREFIX_ROWS, D);
@@ -108,19 +111,23 @@ prefix_attention_kernel(const __grid_constant__ CUtensorMap tmap_k,
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_addr(smem);
-    const uint32_t q_s = sbase + L::Q_OFF, ring_s = sbase + L::RING_OFF, p_s = sbase + L::P_OFF;
+    const uint32_t q_s = sbase + L::Q_OFF, k_ring = sbase + L::K_OFF, v_ring = sbase + L::V_OFF;
     float* red = reinterpret_cast<float*>(smem + L::RED_OFF);
     const uint32_t bar0 = sbase + L::BAR_OFF;
-    // barriers: K/V chunk landed, K/V stage free, S tile ready, S buffer read, P tile
-    // written, P buffer free (its P.V done), row-quarter exchange, all MMAs done
-    auto kv_full = [&](int st) { return bar0 + 8 * st; };
-    auto kv_empty = [&](int st) { return bar0 + 8 * (NS + st); };
-    auto s_full = [&](int b) { return bar0 + 8 * (2 * NS + b); };
-    auto s_free = [&](int b) { return bar0 + 8 * (2 * NS + 2 + b); };
-    auto p_full = [&](int b) { return bar0 + 8 * (2 * NS + 4 + b); };
-    auto p_free = [&](int b) { return bar0 + 8 * (2 * NS + 6 + b); };
-    auto xbar = [&](int qtr, int b) { return bar0 + 8 * (2 * NS + 8 + 2 * qtr + b); };
-    const uint32_t o_done = bar0 + 8 * (2 * NS + 16);
+    // barriers: K / V chunk landed and stage free; S tile ready; S/P buffer free (the
+    // P.V that read it is done); P tile written; row-quarter exchange; all MMAs done;
+    // Q tile stored
+    auto k_full = [&](int st) { return bar0 + 8 * st; };
+    auto k_empty = [&](int st) { return bar0 + 8 * (NK + st); };
+    auto v_full = [&](int st) { return bar0 + 8 * (2 * NK + st); };
+    auto v_empty = [&](int st) { return bar0 + 8 * (2 * NK + NV + st); };
+    constexpr int NB = 2 * NK + 2 * NV;
+    auto s_full = [&](int b) { return bar0 + 8 * (NB + b); };
+    auto s_free = [&](int b) { return bar0 + 8 * (NB + 2 + b); };
+    auto p_full = [&](int b) { return bar0 + 8 * (NB + 4 + b); };
+    auto xbar = [&](int qtr, int b) { return bar0 + 8 * (NB + 6 + 2 * qtr + b); };
+    const uint32_t o_done = bar0 + 8 * (NB + 14);
+    const uint32_t q_full = bar0 + 8 * (NB + 15);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::TMEM_SLOT_OFF);
 
     const int kvh = blockIdx.x, tile = blockIdx.y, split = blockIdx.z;
@@ -133,131 +140,130 @@ prefix_attention_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int n_chunks = t_end > t_begin ? (t_end - t_begin + PREFIX_CHUNK - 1) / PREFIX_CHUNK : 0;
 
     if (threadIdx.x == 0) {
-        for (int st = 0; st < NS; ++st) {
-            mbar_init(kv_full(st), 1);
-            mbar_init(kv_empty(st), 1);
+        for (int st = 0; st < NK; ++st) {
+            mbar_init(k_full(st), 1);
+            mbar_init(k_empty(st), 1);
+        }
+        for (int st = 0; st < NV; ++st) {
+            mbar_init(v_full(st), 1);
+            mbar_init(v_empty(st), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(s_full(b), 1);
-            mbar_init(s_free(b), 8);
+            mbar_init(s_free(b), 1);
             mbar_init(p_full(b), 8);
-            mbar_init(p_free(b), 1);
             for (int qtr = 0; qtr < 4; ++qtr) mbar_init(xbar(qtr, b), 2);
         }
         mbar_init(o_done, 1);
+        mbar_init(q_full, 8);
         mbar_init_fence();
     }
     if (warp == MMA_WARP) umma::alloc(smem_addr(tmem_slot), L::TMEM_COLS);
 
-    // every sequence of this tile must hold the same prefix blocks as sequence 0
-    if (kvh == 0 && split == 0) {
-        const int nb = p.prefix_len / B;
-        const int s_lo = tile * PREFIX_ROWS / G;
-        const int s_hi = min(p.num_seqs, (tile * PREFIX_ROWS + PREFIX_ROWS - 1) / G + 1);
-        for (int i = threadIdx.x; i < (s_hi - s_lo) * nb; i += blockDim.x) {
-            const int s = s_lo + i / nb, j = i % nb;
-            if (p.block_tables[(size_t)s * p.max_blocks_per_seq + j] != p.block_tables[j])
-                set_error(p.err, PKV_DEVERR_PREFIX);
-        }
-    }
-    // Q tile -> shared memory as the first MMA's A operand (rows past the batch are zero)
-    if (warp < 8) {
-        const int i = threadIdx.x & (PREFIX_ROWS - 1), h = threadIdx.x >> 7;
-        const int r = tile * PREFIX_ROWS + i;
-        const long long qr =
-            r < rows ? (long long)(r / G) * p.num_q_heads + (long long)kvh * G + r % G : -1;
-        const uint4* src =
-            reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + (qr < 0 ? 0 : qr) * D);
-        constexpr int HALF = D / 16;  // 16-byte columns per half row
-#pragma unroll
-        for (int c = h * HALF; c < (h + 1) * HALF; ++c) {
-            const uint4 v = qr >= 0 ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(smem + L::Q_OFF + (c / 8) * L::Q_BOX + swz(i, c % 8)) = v;
-        }
-        umma::fence_smem_to_async();
-    }
     umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == COPY_WARP) {
-        // ---- copies: each chunk's pages, once its stage has been released
-        if (lane == 0) {
-            const uint64_t policy = l2_evict_last_policy();  // every tile of the head re-reads them
-            int issued = 0;
-            for (int j = 0; j < n_chunks; ++j) {
-                const int st = j % NS;
-                if (j >= NS && !mbar_wait(kv_empty(st), ((j / NS) - 1) & 1)) {
-                    set_error(p.err, PKV_DEVERR_TIMEOUT);
+    if (warp == K_WARP || warp == V_WARP) {
+        // ---- copies of one pool's pages, each chunk once its stage has been released.
+        // The whole warp runs the loop: its lanes fetch the block ids of 32 boxes (8
+        // chunks) at a time, one window ahead, and lane 0 issues the copies.
+        const bool is_k = warp == K_WARP;
+        const int NST = is_k ? NK : NV;
+        const CUtensorMap* map = is_k ? &tmap_k : &tmap_v;
+        const uint32_t ring = is_k ? k_ring : v_ring;
+        const uint64_t policy = l2_evict_last_policy();  // every tile of the head re-reads them
+        const int box0 = t_begin / CHUNK_TOKENS, nbox = (t_end - t_begin) / CHUNK_TOKENS;
+        auto window_ids = [&](int win) -> int {
+            const int b = win * 32 + lane;
+            return b < nbox ? __ldg(p.block_tables + (box0 + b) * CHUNK_TOKENS / B) : -1;
+        };
+        int ids = window_ids(0), ids_next = window_ids(1);
+        int issued = 0;
+        for (int j = 0; j < n_chunks; ++j) {
+            const int st = j % NST;
+            if (j >= NST) {
+                bool free_ = true;
+                if (lane == 0) free_ = mbar_wait(is_k ? k_empty(st) : v_empty(st), ((j / NST) - 1) & 1);
+                if (!__shfl_sync(FULL_MASK, free_, 0)) {
+                    if (lane == 0) set_error(p.err, PKV_DEVERR_TIMEOUT);
                     break;
                 }
-                const int t0 = t_begin + j * PREFIX_CHUNK;
-                const int boxes = min(PREFIX_CHUNK, t_end - t0) / CHUNK_TOKENS;
-                int row[PREFIX_CHUNK / CHUNK_TOKENS];
-                int good = 0;
+            }
+            if (j > 0 && j % 8 == 0) {
+                ids = ids_next;
+                ids_next = window_ids(j / 8 + 1);
+            }
+            const int t0 = t_begin + j * PREFIX_CHUNK;
+            const int boxes = min(PREFIX_CHUNK, t_end - t0) / CHUNK_TOKENS;
+            int row[PREFIX_CHUNK / CHUNK_TOKENS];
+            int good = 0;
 #pragma unroll
-                for (int b = 0; b < PREFIX_CHUNK / CHUNK_TOKENS; ++b) {
-                    row[b] = -1;
-                    if (b >= boxes) continue;
-                    const int t = t0 + b * CHUNK_TOKENS;
-                    const int phys = __ldg(p.block_tables + t / B);
-                    if ((unsigned)phys >= (unsigned)p.num_blocks) {
-                        set_error(p.err, PKV_DEVERR_BLOCK_ID);  // that piece is not loaded
-                    } else {
-                        row[b] = (phys * p.num_kv_heads + kvh) * B + (t % B);
-                        ++good;
-                    }
+            for (int b = 0; b < PREFIX_CHUNK / CHUNK_TOKENS; ++b) {
+                const int phys = __shfl_sync(FULL_MASK, ids, (j % 8) * 4 + b);
+                row[b] = -1;
+                if (b >= boxes) continue;
+                if ((unsigned)phys >= (unsigned)p.num_blocks) {
+                    if (is_k && lane == 0) set_error(p.err, PKV_DEVERR_BLOCK_ID);  // not loaded
+                } else {
+                    row[b] = (phys * p.num_kv_heads + kvh) * B + (t0 + b * CHUNK_TOKENS) % B;
+                    ++good;
                 }
-                const uint32_t bar = kv_full(st);
-                mbar_arrive_expect_tx(bar, (uint32_t)good * 2 * L::BOXES * CHUNK_TOKENS * 128);
-                const uint32_t dst = ring_s + st * L::STAGE_BYTES;
+            }
+            if (lane == 0) {
+                const uint32_t bar = is_k ? k_full(st) : v_full(st);
+                mbar_arrive_expect_tx(bar, (uint32_t)good * L::BOXES * CHUNK_TOKENS * 128);
+                const uint32_t dst = ring + st * L::STAGE_BYTES;
 #pragma unroll
                 for (int b = 0; b < PREFIX_CHUNK / CHUNK_TOKENS; ++b) {
                     if (row[b] < 0) continue;
 #pragma unroll
-                    for (int x = 0; x < L::BOXES; ++x) {
-                        const uint32_t off = x * L::KV_BOX + b * CHUNK_TOKENS * 128;
-                        tma_load_2d(dst + off, &tmap_k, x * 64, row[b], bar, policy);
-                        tma_load_2d(dst + L::POOL_BYTES + off, &tmap_v, x * 64, row[b], bar, policy);
-                    }
+                    for (int x = 0; x < L::BOXES; ++x)
+                        tma_load_2d(dst + x * L::KV_BOX + b * CHUNK_TOKENS * 128, map, x * 64,
+                                    row[b], bar, policy);
                 }
-                issued = j + 1;
             }
-            // the CTA must not end with copies still landing in its shared memory
-            for (int j = issued > NS ? issued - NS : 0; j < issued; ++j)
-                mbar_wait(kv_full(j % NS), (j / NS) & 1);
+            issued = j + 1;
         }
+        // the CTA must not end with copies still landing in its shared memory
+        if (lane == 0)
+            for (int j = issued > NST ? issued - NST : 0; j < issued; ++j)
+                mbar_wait(is_k ? k_full(j % NST) : v_full(j % NST), (j / NST) & 1);
         __syncwarp();
     } else if (warp == MMA_WARP) {
         // ---- MMA issue: S_j as soon as K_j is in, then the P.V of chunk j - 1
         if (lane == 0) {
             auto issue_pv = [&](int i) -> bool {
-                if (!mbar_wait(p_full(i & 1), (i >> 1) & 1)) return false;
+                if (!mbar_wait(v_full(i % NV), (i / NV) & 1) ||
+                    !mbar_wait(p_full(i & 1), (i >> 1) & 1))
+                    return false;
                 umma::fence_after_sync();
                 const int vt = min(PREFIX_CHUNK, t_end - (t_begin + i * PREFIX_CHUNK));
-                const uint32_t v_s = ring_s + (i % NS) * L::STAGE_BYTES + L::POOL_BYTES;
-                const uint32_t ph = p_s + (i & 1) * 2 * L::P_BYTES, pl = ph + L::P_BYTES;
+                const uint32_t v_s = v_ring + (i % NV) * L::STAGE_BYTES;
+                const uint32_t p_t = tmem + (i & 1) * PREFIX_CHUNK;
                 for (int kk = 0; kk < vt / 16; ++kk) {
-                    // V is N-major: 64-dim blocks KV_BOX apart, 8-token groups 1024 apart
+                    // V is N-major: 64-dim blocks KV_BOX apart, 8-token groups 1024 apart.
+                    // P's 16 tokens of step kk: half kk / 2, its columns 8 (kk % 2) .. + 7
+                    // (high part) and 16 further (remainder)
                     const uint64_t bv = umma::sw128_desc(v_s + kk * 16 * 128, L::KV_BOX, 1024);
-                    umma::mma_f16(tmem + L::O_COL, umma::sw128_desc(ph + kk * 32, 16, 1024), bv,
-                                  IDESC_O, (i > 0 || kk > 0) ? 1u : 0u);
-                    umma::mma_f16(tmem + L::O_COL, umma::sw128_desc(pl + kk * 32, 16, 1024), bv,
-                                  IDESC_O, 1u);
+                    const uint32_t a = p_t + (kk >> 1) * 32 + (kk & 1) * 8;
+                    umma::mma_f16_tmem_a(tmem + L::O_COL, a, bv, IDESC_O,
+                                         (i > 0 || kk > 0) ? 1u : 0u);
+                    umma::mma_f16_tmem_a(tmem + L::O_COL, a + 16, bv, IDESC_O, 1u);
                 }
-                umma::commit(p_free(i & 1));
-                umma::commit(kv_empty(i % NS));
+                umma::commit(s_free(i & 1));
+                umma::commit(v_empty(i % NV));
                 return true;
             };
-            bool ok = true;
+            bool ok = mbar_wait(q_full, 0);
             for (int j = 0; j < n_chunks && ok; ++j) {
-                const int st = j % NS;
-                ok = mbar_wait(kv_full(st), (j / NS) & 1) &&
+                const int st = j % NK;
+                ok = mbar_wait(k_full(st), (j / NK) & 1) &&
                      (j < 2 || mbar_wait(s_free(j & 1), ((j - 2) >> 1) & 1));
                 if (!ok) break;
                 umma::fence_after_sync();
-                const uint32_t k_s = ring_s + st * L::STAGE_BYTES;
+                const uint32_t k_s = k_ring + st * L::STAGE_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < KS; ++kk) {
                     const uint64_t a =
@@ -267,6 +273,7 @@ prefix_attention_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     umma::mma_f16(tmem + (j & 1) * PREFIX_CHUNK, a, b, IDESC_S, kk > 0 ? 1u : 0u);
                 }
                 umma::commit(s_full(j & 1));
+                umma::commit(k_empty(st));
                 if (j >= 1) ok = issue_pv(j - 1);
             }
             if (ok && n_chunks > 0) ok = issue_pv(n_chunks - 1);
@@ -276,17 +283,51 @@ prefix_attention_kernel(const __grid_constant__ CUtensorMap tmap_k,
         }
         __syncwarp();
     } else {
-        // ---- softmax: this thread's row i, columns of half h of each S tile
+        // ---- softmax warps.  First the Q tile, as the first MMA's A operand (rows past
+        // the batch are zero); thread t stores half t / 128 of row t % 128.
         const int qtr = warp & 3, h = warp >> 2;
         const int i = qtr * 32 + lane;
+        {
+            const int r = tile * PREFIX_ROWS + i;
+            const long long qr =
+                r < rows ? (long long)(r / G) * p.num_q_heads + (long long)kvh * G + r % G : -1;
+            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
+                                                              (qr < 0 ? 0 : qr) * D);
+            constexpr int HALF = D / 16;  // 16-byte columns per half row
+            uint4 v[HALF];
+#pragma unroll
+            for (int c = 0; c < HALF; ++c)
+                v[c] = qr >= 0 ? __ldg(src + h * HALF + c) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int c = 0; c < HALF; ++c) {
+                const int cc = h * HALF + c;
+                *reinterpret_cast<uint4*>(smem + L::Q_OFF + (cc / 8) * L::Q_BOX + swz(i, cc % 8)) = v[c];
+            }
+            umma::fence_smem_to_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(q_full);
+        }
+        // Every sequence must hold sequence 0's prefix blocks: this CTA checks the blocks
+        // of its split for the sequences of its tile numbered kvh modulo num_kv_heads.
+        {
+            const int s_lo = tile * PREFIX_ROWS / G;
+            const int s_hi = min(p.num_seqs, (tile * PREFIX_ROWS + PREFIX_ROWS - 1) / G + 1);
+            const int j_lo = t_begin / B, nb = (t_end - t_begin) / B;
+            const int ns = (s_hi - s_lo - kvh + p.num_kv_heads - 1) / p.num_kv_heads;
+            for (int e = threadIdx.x; e < ns * nb; e += 8 * 32) {
+                const int s = s_lo + kvh + (e / nb) * p.num_kv_heads, j = j_lo + e % nb;
+                if (__ldg(p.block_tables + (size_t)s * p.max_blocks_per_seq + j) !=
+                    __ldg(p.block_tables + j))
+                    set_error(p.err, PKV_DEVERR_PREFIX);
+            }
+        }
+        // ---- softmax: this thread's row i, columns of half h of each S tile
         const uint32_t lane_tmem = tmem + ((uint32_t)(qtr * 32) << 16);
-        unsigned char* p_g = smem + L::P_OFF;
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         // the two warps of a row quarter swap one float per row through shared memory
         auto exchange = [&](int j, float v) -> float {
             red[((j & 1) * 2 + h) * PREFIX_ROWS + i] = v;
-            __threadfence_block();
             __syncwarp();
             if (lane == 0) mbar_arrive(xbar(qtr, j & 1));
             if (!__all_sync(FULL_MASK, mbar_wait(xbar(qtr, j & 1), (j >> 1) & 1))) {
@@ -302,11 +343,9 @@ prefix_attention_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 break;
             }
             umma::fence_after_sync();
+            const uint32_t sp = lane_tmem + (j & 1) * PREFIX_CHUNK + h * 32;  // S, then P
             float s[32];
-            umma::ld32(lane_tmem + (j & 1) * PREFIX_CHUNK + h * 32, s);
-            umma::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s_free(j & 1));
+            umma::ld32(sp, s);
             // columns past the chunk's last token hold no key: they take no part
             const int nvalid = vt - h * 32;
             float cm = -INFINITY;
@@ -324,35 +363,22 @@ prefix_attention_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 m_ref = cm;
                 l *= alpha;
             }
+            // P over this half's 32 columns of S: 16 columns of high parts, then 16 of
+            // remainders, two tokens per column
+            uint32_t hi[16], lo[16];
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                s[k] = k < nvalid ? fast_exp2(s[k] - m_ref) : 0.f;
-                l += s[k];
+            for (int k = 0; k < 32; k += 2) {
+                const float a = k < nvalid ? fast_exp2(s[k] - m_ref) : 0.f;
+                const float b = k + 1 < nvalid ? fast_exp2(s[k + 1] - m_ref) : 0.f;
+                l += a + b;
+                hi[k / 2] = Mma<T>::pack(a, b);
+                lo[k / 2] = Mma<T>::pack(a - Mma<T>::round_trip(a), b - Mma<T>::round_trip(b));
             }
-            // the P buffer is free once the P.V of chunk j - 2 is done
-            if (j >= 2 && !__all_sync(FULL_MASK, mbar_wait(p_free(j & 1), ((j - 2) >> 1) & 1))) {
-                ok = false;
-                break;
-            }
-            unsigned char* ph = p_g + (j & 1) * 2 * L::P_BYTES;
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {  // 8 tokens per 16-byte column
-                uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float a = s[cc * 8 + 2 * e], b = s[cc * 8 + 2 * e + 1];
-                    hi[e] = Mma<T>::pack(a, b);
-                    lo[e] = Mma<T>::pack(a - Mma<T>::round_trip(a), b - Mma<T>::round_trip(b));
-                }
-                const uint32_t off = swz(i, h * 4 + cc);
-                *reinterpret_cast<uint4*>(ph + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4*>(ph + L::P_BYTES + off) =
-                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
-            }
-            umma::fence_smem_to_async();
+            umma::st16(sp, hi);
+            umma::st16(sp + 16, lo);
             // rows whose reference rose: scale their O (complete through chunk j - 1)
             if (j >= 1 && __any_sync(FULL_MASK, need)) {
-                if (!__all_sync(FULL_MASK, mbar_wait(p_free((j - 1) & 1), ((j - 1) >> 1) & 1))) {
+                if (!__all_sync(FULL_MASK, mbar_wait(s_free((j - 1) & 1), ((j - 1) >> 1) & 1))) {
                     ok = false;
                     break;
                 }
@@ -365,8 +391,8 @@ prefix_attention_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     for (int k = 0; k < 32; ++k) o[k] *= alpha;
                     umma::st32(lane_tmem + L::O_COL + h * (D / 2) + c, o);
                 }
-                umma::wait_st();
             }
+            umma::wait_st();
             umma::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full(j & 1));
