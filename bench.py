@@ -555,6 +555,316 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ the other rows of the path
+
+def _time_steps(device, stream, steps, warmup, prepare, body):
+    """warm-up, then `steps` timed calls of body() with CUDA events on `stream`; mean ms."""
+    for i in range(warmup):
+        prepare(i)
+        body()
+    torch.cuda.synchronize(device)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    with ClockSampler(device.index) as clocks:
+        for i in range(steps):
+            prepare(i)
+            evs[i][0].record(stream)
+            body()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize(device)
+    if not steps:
+        return 0.0, None
+    return sum(a.elapsed_time(b) for a, b in evs) / steps, clocks.summary()
+
+
+def _base_line(args, metric, value, unit, ms, dtype, config, roofline, cpu, e2e, launches, clocks,
+               higher=True):
+    return {"metric": metric, "value": round(value, 3), "unit": unit, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+            "higher_is_better": higher, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
+            "data": "synthetic", "config": config, "roofline": roofline, "cpu_baseline": cpu,
+            "e2e": e2e, "gpu_launches": launches, "clocks": clocks}
+
+
+def run_multi(args):
+    """Several new tokens per sequence (a speculative draft being verified, or a chunked
+    prefill's tail): slot mapping and cache write of all of them, then the causal
+    multi-query paged decode.  value = algorithmic bytes / step time."""
+    import oracle
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    from paged_kv_cache_293_gb300 import _build
+    _build.build()
+    from paged_kv_cache_293_gb300 import pagedkv as P
+    w = workloads.make(args.workload, seed=args.seed, device=device)
+    nq, S = args.queries, w.num_seqs
+    if int(w.context_lens.min()) < nq:
+        raise SystemExit("every context must hold the %d new tokens" % nq)
+    g = torch.Generator(device=device).manual_seed(args.seed + 7)
+    tdt = w.q.dtype
+    q = torch.randn((S, nq, w.num_q_heads, w.head_dim), generator=g, device=device).to(tdt)
+    k_new = torch.randn((S * nq, w.num_kv_heads, w.head_dim), generator=g, device=device).to(tdt)
+    v_new = torch.randn((S * nq, w.num_kv_heads, w.head_dim), generator=g, device=device).to(tdt)
+    i32 = lambda a: torch.as_tensor(np.ascontiguousarray(a, np.int32), device=device)
+    pos_np = (w.context_lens[:, None] - nq + np.arange(nq)[None, :]).reshape(-1)
+    pos, tseq = i32(pos_np), i32(np.repeat(np.arange(S), nq))
+    bt, ctx = i32(w.block_tables), i32(w.context_lens)
+    slots = torch.empty(S * nq, dtype=torch.int64, device=device)
+    out = torch.empty_like(q)
+    mcl = w.max_context_len
+    ws_bytes = P.pkv_decode_workspace_bytes(w.k_pool, S * nq, w.num_q_heads, mcl, 0)
+    ws = P.workspace_tensor(ws_bytes, device) if ws_bytes else None
+    pools = [(w.k_pool, w.v_pool), (w.k_pool.clone(), w.v_pool.clone())]
+    cur = {}
+
+    def prepare(i):
+        cur["k"], cur["v"] = pools[i % 2]
+
+    def body():
+        P.pkv_slot_mapping(bt, pos, w.block_size, slots, token_seq=tseq)
+        P.pkv_kv_cache_write(cur["k"], cur["v"], k_new, v_new, slots)
+        P.pkv_paged_attention_decode_multi(q, cur["k"], cur["v"], bt, ctx, w.scale, out, mcl, 0,
+                                           ws)
+
+    stream = torch.cuda.current_stream(device)
+    ms, clocks = _time_steps(device, stream, args.steps, args.warmup, prepare, body)
+    if P.pkv_get_device_error():
+        raise RuntimeError("device error flags set")
+    e = workloads.ELEM_BYTES[w.dtype]
+    kv = int(w.context_lens.sum()) * accounting.kv_bytes_per_token(w.num_kv_heads, w.head_dim, e)
+    qo = 2 * S * nq * w.num_q_heads * w.head_dim * e
+    table = int(np.ceil(w.context_lens / w.block_size).sum()) * 4
+    write = accounting.write_bytes(S * nq, w.num_kv_heads, w.head_dim, e) + 12 * S * nq
+    total = kv + qo + table + write    # partition partials not counted
+    peak, peak_kind = read_peaks()
+
+    # the same step end to end: q and the new rows in from pinned host memory, out back
+    h_in = [t.cpu().pin_memory() for t in (q, k_new, v_new)]
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    d_in = (q, k_new, v_new)
+
+    def e2e_body():
+        for d, h in zip(d_in, h_in):
+            d.copy_(h, non_blocking=True)
+        body()
+        h_out.copy_(out, non_blocking=True)
+
+    e2e_ms, _ = _time_steps(device, stream, max(3, args.steps // 4), 3, prepare, e2e_body)
+    h2d = sum(h.numel() * h.element_size() for h in h_in)
+    d2h = h_out.numel() * h_out.element_size()
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        k_h, v_h = workloads.storage_numpy(pools[0][0]), workloads.storage_numpy(pools[0][1])
+        q_h = workloads.storage_numpy(q)
+        n = S
+        t = time.perf_counter()
+        oracle.paged_decode_multi(w.dtype, k_h, v_h, q_h[:2], w.block_tables[:2],
+                                  w.context_lens[:2], w.scale)
+        per_tok = (time.perf_counter() - t) / max(1, int(w.context_lens[:2].sum()))
+        while n > 1 and per_tok * int(w.context_lens[:n].sum()) > 15.0:
+            n //= 2
+        t = time.perf_counter()
+        oracle.paged_decode_multi(w.dtype, k_h, v_h, q_h[:n], w.block_tables[:n],
+                                  w.context_lens[:n], w.scale)
+        sec = time.perf_counter() - t
+        b = int(w.context_lens[:n].sum()) * accounting.kv_bytes_per_token(
+            w.num_kv_heads, w.head_dim, e)
+        cpu = {"value": round(b / sec / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+               "kind": "oracle", "tokens_per_s_per_layer": round(n * nq / sec, 2),
+               "sample": "first %d of %d sequences, %d queries each, one pass of %.2f s, fp64 C "
+                         "with OpenMP" % (n, S, nq, sec)}
+    dec_name = "paged_decode_mma_kernel" if (w.dtype != "f32") else "paged_decode_kernel"
+    line = _base_line(
+        args, "multi-query paged decode HBM GB/s and new tokens/s per layer",
+        total / (ms * 1e-3) / 1e9, "GB/s", ms, w.dtype,
+        {"workload": w.name + "_q%d" % nq, "num_seqs": S, "queries_per_seq": nq,
+         "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+         "block_size": w.block_size, "context_lens": LENGTH_RECIPES.get(args.workload, ""),
+         "kv_bytes_per_step": kv, "partition_size": "auto",
+         "l2": "consecutive steps alternate between two KV pools (two layers' caches)",
+         "path": "slot mapping and cache write of the %d new tokens per sequence, causal "
+                 "multi-query decode" % nq},
+        {"kernel": dec_name + " (all launches of the step)", "bound": "hbm",
+         "achieved": round(total / (ms * 1e-3) / 1e9, 2), "peak": peak, "unit": "GB/s",
+         "frac": round(total / (ms * 1e-3) / 1e9 / peak, 4), "peak_kind": peak_kind,
+         "traffic": None, "algorithmic_bytes": total},
+        cpu,
+        {"value": round(total / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+         "ms_per_step": round(e2e_ms, 5), "overlap": "none: copies, step and read-back in order",
+         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        (3 + (1 if ws_bytes else 0)) * args.steps, clocks)
+    line["tokens_per_s_per_layer"] = round(S * nq / (ms * 1e-3), 1)
+    print(json.dumps(line), flush=True)
+
+
+def run_swap(args):
+    """Preemption swap: a quarter of the batch's blocks out to a pinned host pool and back.
+    The denominator is the same bytes moved by cudaMemcpyAsync between contiguous pinned
+    host memory and the device, measured in the same run."""
+    import oracle
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    from paged_kv_cache_293_gb300 import _build
+    _build.build()
+    from paged_kv_cache_293_gb300 import pagedkv as P
+    w = workloads.make(args.workload, seed=args.seed, device=device)
+    used = np.unique(np.concatenate([w.block_tables[s, :-(-int(c) // w.block_size)]
+                                     for s, c in enumerate(w.context_lens)]))
+    rng = np.random.default_rng(args.seed + 11)
+    moved = np.sort(rng.choice(used, size=max(1, len(used) // 4), replace=False)).astype(np.int32)
+    n = len(moved)
+    shape = (n,) + tuple(w.k_pool.shape[1:])
+    hk = torch.empty(shape, dtype=w.k_pool.dtype).pin_memory()
+    hv = torch.empty(shape, dtype=w.v_pool.dtype).pin_memory()
+    out_pairs = torch.as_tensor(np.stack([moved, np.arange(n, dtype=np.int32)], 1).reshape(-1),
+                                device=device)
+    in_pairs = torch.as_tensor(np.stack([np.arange(n, dtype=np.int32), moved], 1).reshape(-1),
+                               device=device)
+    nbytes = 2 * hk.numel() * hk.element_size()          # both pools, one direction
+    stream = torch.cuda.current_stream(device)
+    idx = torch.as_tensor(moved, device=device).long()
+    before = (w.k_pool[idx].cpu(), w.v_pool[idx].cpu())
+
+    def body():
+        P.pkv_swap_blocks(w.k_pool, w.v_pool, hk, hv, out_pairs)
+        P.pkv_swap_blocks(hk, hv, w.k_pool, w.v_pool, in_pairs)
+
+    ms, clocks = _time_steps(device, stream, args.steps, args.warmup, lambda i: None, body)
+    if P.pkv_get_device_error():
+        raise RuntimeError("device error flags set")
+    same = (torch.equal(w.k_pool[idx].cpu(), before[0])
+            and torch.equal(w.v_pool[idx].cpu(), before[1]))
+    # the link's own rate for the same bytes: contiguous pinned copies each way
+    dk = torch.empty(shape, dtype=w.k_pool.dtype, device=device)
+    dv = torch.empty_like(dk)
+
+    def copies():
+        hk.copy_(dk, non_blocking=True)
+        hv.copy_(dv, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+
+    link_ms, _ = _time_steps(device, stream, args.steps, args.warmup, lambda i: None, copies)
+    value = 2 * nbytes / (ms * 1e-3) / 1e9
+    link = 2 * nbytes / (link_ms * 1e-3) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline:
+        k_h, v_h = workloads.storage_numpy(w.k_pool), workloads.storage_numpy(w.v_pool)
+        hk2 = np.empty((n,) + k_h.shape[1:], k_h.dtype)
+        hv2 = np.empty_like(hk2)
+        pairs = np.stack([moved, np.arange(n, dtype=np.int32)], 1)
+        t = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - t < 5.0 or reps == 0:
+            oracle.swap_blocks(k_h, v_h, hk2, hv2, pairs)
+            reps += 1
+        sec = (time.perf_counter() - t) / reps
+        cpu = {"value": round(nbytes / sec / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": "the same %d blocks copied out on the host (one direction), %d passes"
+                         % (n, reps)}
+    line = _base_line(
+        args, "block swap GPU <-> pinned host GB/s (both directions)", value, "GB/s", ms,
+        w.dtype,
+        {"workload": w.name + "_swap", "blocks_moved": n, "pool_blocks": w.num_blocks,
+         "bytes_each_way": nbytes, "block_choice": "a seeded quarter of the blocks in use",
+         "round_trip_bit_exact": bool(same), "path": "swap out, then swap back in"},
+        {"kernel": "copy_blocks_kernel (two launches)", "bound": "host link",
+         "achieved": round(value, 2), "peak": round(link, 2), "unit": "GB/s",
+         "frac": round(value / link, 4),
+         "peak_kind": "measured in this run: cudaMemcpyAsync of the same bytes, contiguous "
+                      "pinned host <-> device, both directions", "traffic": None,
+         "algorithmic_bytes": 2 * nbytes},
+        cpu,
+        {"value": round(value, 2), "unit": "GB/s", "ms_per_step": round(ms, 5),
+         "note": "the swap moves host buffers by itself: this is the call a user makes",
+         "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes},
+        2 * args.steps, clocks)
+    print(json.dumps(line), flush=True)
+
+
+def run_alloc(args):
+    """Block bookkeeping of one decode step on the device: every sequence grows by one token
+    (a new block where it crosses a block boundary).  Latency-bound; the floor is the
+    library's smallest launch (slot mapping of one token) timed in the same run."""
+    import oracle
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    from paged_kv_cache_293_gb300 import _build
+    _build.build()
+    from paged_kv_cache_293_gb300 import pagedkv as P
+    w = workloads.make(args.workload, seed=args.seed, device=device)
+    S, B = w.num_seqs, w.block_size
+    steps_total = args.warmup + args.steps
+    M = int(-(-(int(w.context_lens.max()) + steps_total) // B)) + 1
+    need = int(np.sum(-(-(w.context_lens + steps_total) // B))) + 16
+    N = max(need, 1024)
+    # a small pool: no block is shared, so no copy-on-write copies are made
+    kp = torch.empty((N, w.num_kv_heads, B, w.head_dim), dtype=w.k_pool.dtype, device=device)
+    vp = torch.empty_like(kp)
+    alloc = P.BlockAllocator(N, device)
+    P.pkv_allocator_reset(alloc)
+    tables = torch.full((S, M), -1, dtype=torch.int32, device=device)
+    status = torch.empty(S, dtype=torch.int32, device=device)
+    i32 = lambda a: torch.as_tensor(np.ascontiguousarray(a, np.int32), device=device)
+    lens = [i32(w.context_lens + i) for i in range(steps_total + 1)]
+    P.pkv_allocate_for_append(alloc, kp, vp, tables, i32(np.zeros(S)), lens[0], status)
+    cur = {}
+
+    def prepare(i):
+        cur["i"] = i
+
+    def body():
+        i = cur["i"]
+        P.pkv_allocate_for_append(alloc, kp, vp, tables, lens[i], lens[i + 1], status)
+
+    stream = torch.cuda.current_stream(device)
+    # warm-up steps 0..W-1, timed steps W..W+K-1
+    ms_w, _ = _time_steps(device, stream, 0, args.warmup, prepare, body)
+    base = args.warmup
+    ms, clocks = _time_steps(device, stream, args.steps, 0, lambda i: prepare(base + i), body)
+    torch.cuda.synchronize(device)
+    ok = bool(torch.all(status == 0)) and not P.pkv_get_device_error()
+    one_tok = torch.zeros(1, dtype=torch.int32, device=device)
+    slot1 = torch.empty(1, dtype=torch.int64, device=device)
+    floor_ms, _ = _time_steps(device, stream, args.steps, args.warmup, lambda i: None,
+                              lambda: P.pkv_slot_mapping(tables[:1], one_tok, B, slot1))
+    new_blocks = int(np.sum(-(-(w.context_lens + steps_total) // B)
+                            - -(-(w.context_lens + base) // B)))
+    cpu = None
+    if not args.no_cpu_baseline:
+        ref = oracle.Allocator(N)
+        k_h = np.zeros((N, 1), np.uint16)   # no block is shared: nothing is copied
+        tb = np.full((S, M), -1, np.int32)
+        ref.allocate_for_append(k_h, k_h, B, tb, np.zeros(S, np.int32),
+                                w.context_lens.astype(np.int32))
+        reps, t = 0, time.perf_counter()
+        while reps < steps_total and (time.perf_counter() - t < 5.0 or reps == 0):
+            ref.allocate_for_append(k_h, k_h, B, tb, (w.context_lens + reps).astype(np.int32),
+                                    (w.context_lens + reps + 1).astype(np.int32))
+            reps += 1
+        sec = (time.perf_counter() - t) / reps
+        cpu = {"value": round(sec * 1e6, 2), "unit": "us per step", "cores": 1, "kind": "oracle",
+               "sample": "the same %d sequences growing one token a step, %d steps (sequential "
+                         "C)" % (S, reps)}
+    line = _base_line(
+        args, "device block bookkeeping: microseconds per decode step's allocate-for-append",
+        ms * 1e3, "us", ms, "int32",
+        {"workload": w.name + "_alloc", "num_seqs": S, "block_size": B, "pool_blocks": N,
+         "blocks_taken_in_timed_steps": new_blocks,
+         "all_statuses_ok": ok,
+         "path": "every sequence grows by one token per step; a fresh block where it crosses a "
+                 "block boundary"},
+        {"kernel": "allocate_for_append_kernel", "bound": "latency", "achieved": round(ms * 1e3, 3),
+         "peak": round(floor_ms * 1e3, 3), "unit": "us", "frac": round(floor_ms / ms, 4),
+         "peak_kind": "measured in this run: one-token slot mapping launch (the library's "
+                      "smallest kernel)", "traffic": None, "algorithmic_bytes": None},
+        cpu,
+        None, args.steps, clocks, higher=False)
+    line["sequences_per_s"] = round(S / (ms * 1e-3), 1)
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -568,7 +878,13 @@ def main():
                     help="how timed steps are kept L2-cold")
     ap.add_argument("--cascade", action="store_true",
                     help="shared-prefix batches: prefix attention once per kv head, then the "
-                         "suffixes, then the merge (slower than plain decode on the batches here)")
+                         "suffixes, then the merge (pays when the shared prefix is long against "
+                         "the suffixes, as on the system-prompt batch)")
+    ap.add_argument("--path", choices=["decode", "multi", "swap", "alloc"], default="decode",
+                    help="decode: the decode step (default); multi: several new tokens per "
+                         "sequence; swap: blocks to pinned host memory and back; alloc: the "
+                         "device block bookkeeping of a step")
+    ap.add_argument("--queries", type=int, default=4, help="new tokens per sequence (--path multi)")
     ap.add_argument("--unfused", action="store_true",
                     help="slot mapping, cache write and decode as three launches")
     args = ap.parse_args()
@@ -576,6 +892,12 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.path == "multi":
+        run_multi(args)
+    elif args.path == "swap":
+        run_swap(args)
+    elif args.path == "alloc":
+        run_alloc(args)
     else:
         run_ours(args)
 
