@@ -604,6 +604,49 @@ def test_cascade_prefix_pass_rescales_when_scores_grow(P):
     assert_no_device_error(P)
 
 
+def test_cascade_long_prefix_few_sequences(P):
+    """A 4096-token prefix shared by three sequences: a few CTAs per kv head, so the
+    prefix is cut into many splits, each its own slot in the merge."""
+    B, nb = 16, 256
+    w = workloads.build("cascade_long", dtype="bf16", num_q_heads=16, num_kv_heads=4,
+                        head_dim=128, block_size=B, context_lens=[nb * B + x for x in (5, 100, 1000)],
+                        seed=55, device=DEV, shared_prefix_blocks=nb)
+    Lp, mcl = nb * B, w.max_context_len
+    ws = P.workspace_tensor(P.pkv_cascade_workspace_bytes(w.k_pool, w.num_seqs, 16, mcl, Lp), DEV)
+    out = torch.full((w.num_seqs, 16, 128), float("nan"), dtype=torch.float32, device=DEV)
+    P.pkv_paged_attention_decode_cascade(w.q, w.k_pool, w.v_pool, dev_i32(w.block_tables),
+                                         dev_i32(w.context_lens), w.scale, out, mcl, Lp, ws)
+    torch.cuda.synchronize()
+    assert max_abs(out, oracle_decode(w)) <= TOL["bf16"]
+    plain = run_decode(P, w)
+    assert max_abs(out, plain.double().cpu().numpy()) <= 1e-5
+    assert_no_device_error(P)
+
+
+def test_cascade_head_dim_64_rescales_when_scores_grow(P):
+    """head_dim 64 (one 128-byte column per row) with keys growing along the prefix,
+    so later chunks raise the reference maximum and rescale the half-width O."""
+    B, nb = 32, 24
+    ctx = [nb * B + x for x in (1, 40, 300)] * 30
+    w = workloads.build("cascade_d64", dtype="f16", num_q_heads=8, num_kv_heads=2, head_dim=64,
+                        block_size=B, context_lens=ctx, seed=56, device=DEV,
+                        shared_prefix_blocks=nb)
+    blocks = torch.as_tensor(w.block_tables[0, :nb].astype(np.int64), device=DEV)
+    t = torch.arange(nb * B, device=DEV, dtype=torch.float32)
+    w.k_pool[blocks] = (w.k_pool[blocks].float() * (1 + 12 * t / (nb * B)).view(nb, 1, B, 1)).to(
+        w.k_pool.dtype)
+    Lp, mcl = nb * B, w.max_context_len
+    ws = P.workspace_tensor(P.pkv_cascade_workspace_bytes(w.k_pool, w.num_seqs, 8, mcl, Lp), DEV)
+    out = torch.full((w.num_seqs, 8, 64), float("nan"), dtype=torch.float32, device=DEV)
+    P.pkv_paged_attention_decode_cascade(w.q, w.k_pool, w.v_pool, dev_i32(w.block_tables),
+                                         dev_i32(w.context_lens), w.scale, out, mcl, Lp, ws)
+    torch.cuda.synchronize()
+    ref = oracle.paged_decode("f16", host(w.k_pool), host(w.v_pool), host(w.q), w.block_tables,
+                              w.context_lens, w.scale)
+    assert max_abs(out, ref) <= TOL["f16"]
+    assert_no_device_error(P)
+
+
 def test_cascade_on_the_system_prompt_batch_matches_oracle(P):
     """The long-shared-prompt batch through bench.py's cascade step, against the oracle."""
     import bench
