@@ -284,24 +284,31 @@ prefix_attention_kernel(const __grid_constant__ CUtensorMap tmap_k,
         __syncwarp();
     } else {
         // ---- softmax warps.  First the Q tile, as the first MMA's A operand (rows past
-        // the batch are zero); thread t stores half t / 128 of row t % 128.
+        // the batch are zero): warp w copies rows 16 w .. 16 w + 15, whole rows per load.
         const int qtr = warp & 3, h = warp >> 2;
         const int i = qtr * 32 + lane;
+        auto q_index = [&](int r) -> long long {  // tile row -> q row, -1 past the batch
+            const int gr = tile * PREFIX_ROWS + r;
+            return gr < rows ? (long long)(gr / G) * p.num_q_heads + (long long)kvh * G + gr % G
+                             : -1;
+        };
         {
-            const int r = tile * PREFIX_ROWS + i;
-            const long long qr =
-                r < rows ? (long long)(r / G) * p.num_q_heads + (long long)kvh * G + r % G : -1;
-            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
-                                                              (qr < 0 ? 0 : qr) * D);
-            constexpr int HALF = D / 16;  // 16-byte columns per half row
-            uint4 v[HALF];
+            constexpr int CPR = D / 8;                // 16-byte columns per row
+            constexpr int RPL = 32 / CPR;             // rows per warp load
+            constexpr int LOADS = 16 / RPL;
+            const int c = lane % CPR;
+            uint4 v[LOADS];
 #pragma unroll
-            for (int c = 0; c < HALF; ++c)
-                v[c] = qr >= 0 ? __ldg(src + h * HALF + c) : make_uint4(0u, 0u, 0u, 0u);
+            for (int k = 0; k < LOADS; ++k) {
+                const long long qr = q_index(warp * 16 + k * RPL + lane / CPR);
+                v[k] = qr >= 0 ? __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
+                                                                      qr * D) + c)
+                               : make_uint4(0u, 0u, 0u, 0u);
+            }
 #pragma unroll
-            for (int c = 0; c < HALF; ++c) {
-                const int cc = h * HALF + c;
-                *reinterpret_cast<uint4*>(smem + L::Q_OFF + (cc / 8) * L::Q_BOX + swz(i, cc % 8)) = v[c];
+            for (int k = 0; k < LOADS; ++k) {
+                const int r = warp * 16 + k * RPL + lane / CPR;
+                *reinterpret_cast<uint4*>(smem + L::Q_OFF + (c / 8) * L::Q_BOX + swz(r, c % 8)) = v[k];
             }
             umma::fence_smem_to_async();
             __syncwarp();
@@ -401,35 +408,46 @@ prefix_attention_kernel(const __grid_constant__ CUtensorMap tmap_k,
             ok = __all_sync(FULL_MASK, mbar_wait(o_done, 0));
             if (ok) l += exchange(n_chunks, l);
         }
-        const int r = tile * PREFIX_ROWS + i;
-        const long long qr =
-            r < rows ? (long long)(r / G) * p.num_q_heads + (long long)kvh * G + r % G : -1;
-        const size_t slot = (size_t)(qr < 0 ? 0 : qr) * p.max_parts + split;
-        float* orow = p.ws_o + slot * D + h * (D / 2);
-        if (ok) {
+        // O leaves through shared memory (the K ring, idle once every MMA is done) so
+        // that each warp then writes whole rows: row r of the staging area holds D floats
+        // at a stride of D + 4 (no bank conflicts between the rows of a warp's store).
+        float* stage = reinterpret_cast<float*>(smem + L::K_OFF);
+        constexpr int SROW = D + 4;
+        if (ok && n_chunks > 0) {
             umma::fence_after_sync();
 #pragma unroll
             for (int c = 0; c < D / 2; c += 32) {
                 float o[32];
-                if (n_chunks > 0) {
-                    umma::ld32(lane_tmem + L::O_COL + h * (D / 2) + c, o);
-                } else {
+                umma::ld32(lane_tmem + L::O_COL + h * (D / 2) + c, o);
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) o[k] = 0.f;
-                }
-                if (qr >= 0) {
-#pragma unroll
-                    for (int k = 0; k < 32; k += 4)
-                        *reinterpret_cast<float4*>(orow + c + k) =
-                            make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
-                }
+                for (int k = 0; k < 32; k += 4)
+                    *reinterpret_cast<float4*>(stage + i * SROW + h * (D / 2) + c + k) =
+                        make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
             }
-            if (qr >= 0 && h == 0) {
-                p.ws_m[slot] = m_ref * 0.69314718055994530942f;  // natural-log units
+        }
+        // every softmax warp reaches this barrier, whatever happened above
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        const bool all_ok = ok && n_chunks > 0;
+        if (!ok && lane == 0) set_error(p.err, PKV_DEVERR_TIMEOUT);
+        {
+            const long long qr = q_index(i);
+            const size_t slot = (size_t)(qr < 0 ? 0 : qr) * p.max_parts + split;
+            if (qr >= 0 && h == 0 && ok) {
+                p.ws_m[slot] = n_chunks > 0 ? m_ref * 0.69314718055994530942f : -INFINITY;
                 p.ws_l[slot] = l;
             }
-        } else if (lane == 0) {
-            set_error(p.err, PKV_DEVERR_TIMEOUT);
+        }
+        if (ok) {
+            constexpr int F4 = D / 4;  // float4 per row
+#pragma unroll 4
+            for (int rr = 0; rr < 16; ++rr) {
+                const int r = warp * 16 + rr;
+                const long long qr = q_index(r);
+                if (qr < 0 || lane >= F4) continue;
+                const float4 v = all_ok ? *reinterpret_cast<const float4*>(stage + r * SROW + lane * 4)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+                reinterpret_cast<float4*>(p.ws_o + ((size_t)qr * p.max_parts + split) * D)[lane] = v;
+            }
         }
     }
 
