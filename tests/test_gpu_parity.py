@@ -516,6 +516,7 @@ def test_bench_step_matches_oracle_at_full_size(P, name):
     ("bf16", 32, 8, 128, 16, 4, [1, 30, 700, 2000, 16], 0),     # tensor-core suffix, G = 4
     ("f16", 8, 8, 128, 32, 3, [5, 64, 1100, 33], 512),         # CUDA-core suffix (MHA), B = 32
     ("f16", 16, 2, 64, 16, 2, [0, 9, 300], 256),               # a sequence that is all prefix
+    ("f16", 8, 8, 128, 16, 2, [0, 7, 100], 0),                 # CUDA-core suffix finishing rows
 ])
 def test_cascade_decode_matches_oracle_and_plain_decode(P, dtype, Hq, Hkv, D, B, prefix_blocks,
                                                         suffix, psize):
