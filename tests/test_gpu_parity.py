@@ -575,6 +575,23 @@ def test_cascade_flags_a_sequence_with_other_prefix_blocks(P):
     assert P.pkv_get_device_error() & P.DEVERR["PREFIX"]
 
 
+def test_cascade_flags_a_prefix_block_outside_the_pool(P):
+    """Every sequence's third prefix block names a block past the pool: the prefix pass
+    copies nothing for it, sets BLOCK_ID, and the call still returns."""
+    w = workloads.build("cascade_badid", dtype="bf16", num_q_heads=8, num_kv_heads=2,
+                        head_dim=128, block_size=16, context_lens=[100, 120], seed=57,
+                        device=DEV, shared_prefix_blocks=4)
+    bt = w.block_tables.copy()
+    bt[:, 2] = w.num_blocks + 5
+    ws = P.workspace_tensor(P.pkv_cascade_workspace_bytes(w.k_pool, 2, 8, 120, 64), DEV)
+    out = torch.empty((2, 8, 128), dtype=torch.float32, device=DEV)
+    P.pkv_paged_attention_decode_cascade(w.q, w.k_pool, w.v_pool, dev_i32(bt),
+                                         dev_i32(w.context_lens), w.scale, out, 120, 64, ws)
+    torch.cuda.synchronize()
+    flags = P.pkv_get_device_error()
+    assert flags & P.DEVERR["BLOCK_ID"] and not flags & P.DEVERR["TIMEOUT"]
+
+
 def test_cascade_prefix_pass_rescales_when_scores_grow(P):
     """Keys scaled by 1 + 15 t / 640 along a 640-token shared prefix: each row's
     maximum keeps rising, so the prefix pass raises its reference maximum and
