@@ -447,7 +447,7 @@ CascadeShape cascade_shape(const pkv_pool* pool, int32_t num_seqs, int32_t num_q
     for (int32_t s = 1; s <= std::min<int32_t>(chunks, 64); ++s) {
         const int32_t cps = ceil_div(chunks, s);
         const int64_t splits = ceil_div(chunks, cps);
-        const int64_t waves = (ctas * splits + sms - 1) / sms;
+        const int64_t waves = (ctas * splits + 2 * sms - 1) / (2 * sms);  // two CTAs per SM
         const int64_t cost = waves * (cps + 3);
         if (cost < best_cost) {
             best_cost = cost;

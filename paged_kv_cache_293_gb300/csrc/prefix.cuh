@@ -43,8 +43,9 @@
 
 namespace pkv {
 
-constexpr int PREFIX_K_STAGES = 6;
-constexpr int PREFIX_V_STAGES = 5;
+constexpr int PREFIX_K_STAGES = 2;
+constexpr int PREFIX_V_STAGES = 2;
+constexpr int PREFIX_CTAS_PER_SM = 2;
 constexpr int PREFIX_ROWS = 128;     // query rows per CTA
 constexpr int PREFIX_CHUNK = 64;     // prefix tokens per S tile
 constexpr int PREFIX_THREADS = 352;  // 8 softmax warps, K copies, MMA issue, V copies
@@ -97,7 +98,7 @@ __device__ __forceinline__ uint64_t l2_evict_last_policy() {
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(PREFIX_THREADS, 1)
+__global__ void __launch_bounds__(PREFIX_THREADS, PREFIX_CTAS_PER_SM)
 prefix_attention_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v, const PrefixParams p) {
     using L = PrefixSmem<D>;
