@@ -170,15 +170,25 @@ __global__ void __launch_bounds__(256) lse_merge_rows_kernel(const MergeParams p
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long row = (long long)blockIdx.x * 8 + warp;
     if (row >= rows) return;
-    const int n = merge_parts(p, row);
-    if (p.skip_single && n <= 1) return;
     const float* mrow = p.ws_m + (size_t)row * p.max_parts;
     const float* lrow = p.ws_l + (size_t)row * p.max_parts;
     const float* orow = p.ws_o + (size_t)row * p.max_parts * D;
+    // every load at once (all max_parts <= 8 slots of the row; the ones past this row's
+    // partition count are read and then ignored), so the row costs one memory round trip
     float lk = 0.f, mk = -INFINITY;
-    if (lane < n) {
+    if (lane < p.max_parts) {
         lk = lrow[lane];
-        mk = lk > 0.f ? mrow[lane] : -INFINITY;
+        mk = mrow[lane];
+    }
+    float v[8][V];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        if (k < p.max_parts) MergeVec<D>::load(orow + (size_t)k * D + lane * V, v[k]);
+    const int n = merge_parts(p, row);
+    if (p.skip_single && n <= 1) return;
+    if (lane >= n || !(lk > 0.f)) {
+        lk = 0.f;
+        mk = -INFINITY;
     }
     float M = mk;
 #pragma unroll
@@ -196,13 +206,13 @@ __global__ void __launch_bounds__(256) lse_merge_rows_kernel(const MergeParams p
     float acc[V];
 #pragma unroll
     for (int j = 0; j < V; ++j) acc[j] = 0.f;
-#pragma unroll 8
-    for (int k = 0; k < n; ++k) {
-        const float wk = __shfl_sync(FULL_MASK, w, k);
-        float v[V];
-        MergeVec<D>::load(orow + (size_t)k * D + lane * V, v);
 #pragma unroll
-        for (int j = 0; j < V; ++j) acc[j] = fmaf(wk, v[j], acc[j]);
+    for (int k = 0; k < 8; ++k) {
+        const float wk = __shfl_sync(FULL_MASK, w, k);
+        if (k < n) {
+#pragma unroll
+            for (int j = 0; j < V; ++j) acc[j] = fmaf(wk, v[k][j], acc[j]);
+        }
     }
 #pragma unroll
     for (int j = 0; j < V; ++j) store_out(p.out, p.out_dtype, out_base + j, acc[j] / L);
