@@ -218,11 +218,11 @@ __global__ void __launch_bounds__(256) lse_merge_rows_kernel(const MergeParams p
     for (int j = 0; j < V; ++j) store_out(p.out, p.out_dtype, out_base + j, acc[j] / L);
 }
 
-// Many partitions: one CTA of 8 warps per row; warp w takes partitions w, w + 8, ...
-// with several loads in flight, and the warps' sums meet in shared memory.
+// Many partitions: one CTA of 16 warps per row; warp w takes partitions w, w + 16, ...
+// with eight loads in flight, and the warps' sums meet in shared memory.
 template <int D>
-__global__ void __launch_bounds__(256) lse_merge_kernel(const MergeParams p) {
-    constexpr int NWM = 8, V = MergeVec<D>::N;
+__global__ void __launch_bounds__(512) lse_merge_kernel(const MergeParams p) {
+    constexpr int NWM = 16, V = MergeVec<D>::N;
     __shared__ float red[NWM][D + 1];
     __shared__ float smax[NWM];
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const MergeParams p) {
     float L = 0.f, acc[V];
 #pragma unroll
     for (int j = 0; j < V; ++j) acc[j] = 0.f;
-#pragma unroll 4
+#pragma unroll 8
     for (int k = warp; k < n; k += NWM) {
         const float lk = lrow[k];
         const float wk = lk > 0.f ? fast_exp2((mrow[k] - M) * 1.4426950408889634f) : 0.f;
@@ -280,7 +280,7 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
     const bool few = p.max_parts <= 8;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(few ? (unsigned)((rows + 7) / 8) : (unsigned)rows);
-    cfg.blockDim = dim3(256);
+    cfg.blockDim = dim3(few ? 256 : 512);  // 8 rows of one warp each, or 16 warps on one row
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
