@@ -588,8 +588,9 @@ def _base_line(args, metric, value, unit, ms, dtype, config, roofline, cpu, e2e,
 
 def run_multi(args):
     """Several new tokens per sequence (a speculative draft being verified, or a chunked
-    prefill's tail): slot mapping and cache write of all of them, then the causal
-    multi-query paged decode.  value = algorithmic bytes / step time."""
+    prefill's tail): their K/V rows written into the cache and the causal multi-query paged
+    decode, in one launch (with --unfused: slot mapping, cache write, then the decode).
+    value = algorithmic bytes / step time."""
     import oracle
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
@@ -620,11 +621,17 @@ def run_multi(args):
     def prepare(i):
         cur["k"], cur["v"] = pools[i % 2]
 
-    def body():
+    def body_unfused():
         P.pkv_slot_mapping(bt, pos, w.block_size, slots, token_seq=tseq)
         P.pkv_kv_cache_write(cur["k"], cur["v"], k_new, v_new, slots)
         P.pkv_paged_attention_decode_multi(q, cur["k"], cur["v"], bt, ctx, w.scale, out, mcl, 0,
                                            ws)
+
+    def body_fused():
+        P.pkv_paged_attention_decode_multi_append(q, cur["k"], cur["v"], k_new, v_new, bt, ctx,
+                                                  w.scale, out, mcl, 0, ws, slot_mapping=slots)
+
+    body = body_unfused if args.unfused else body_fused
 
     stream = torch.cuda.current_stream(device)
     ms, clocks = _time_steps(device, stream, args.steps, args.warmup, prepare, body)
@@ -683,8 +690,10 @@ def run_multi(args):
          "block_size": w.block_size, "context_lens": LENGTH_RECIPES.get(args.workload, ""),
          "kv_bytes_per_step": kv, "partition_size": "auto",
          "l2": "consecutive steps alternate between two KV pools (two layers' caches)",
-         "path": "slot mapping and cache write of the %d new tokens per sequence, causal "
-                 "multi-query decode" % nq},
+         "path": ("slot mapping and cache write of the %d new tokens per sequence, causal "
+                  "multi-query decode" % nq) if args.unfused else
+                 ("the %d new tokens per sequence written into the cache by the causal "
+                  "multi-query decode launch itself" % nq)},
         {"kernel": dec_name + " (all launches of the step)", "bound": "hbm",
          "achieved": round(total / (ms * 1e-3) / 1e9, 2), "peak": peak, "unit": "GB/s",
          "frac": round(total / (ms * 1e-3) / 1e9 / peak, 4), "peak_kind": peak_kind,
@@ -693,7 +702,7 @@ def run_multi(args):
         {"value": round(total / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
          "ms_per_step": round(e2e_ms, 5), "overlap": "none: copies, step and read-back in order",
          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        (3 + (1 if ws_bytes else 0)) * args.steps, clocks)
+        ((3 if args.unfused else 1) + (1 if ws_bytes else 0)) * args.steps, clocks)
     line["tokens_per_s_per_layer"] = round(S * nq / (ms * 1e-3), 1)
     print(json.dumps(line), flush=True)
 

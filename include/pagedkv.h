@@ -212,6 +212,31 @@ pkv_status pkv_paged_attention_decode_multi(
     void* stream);
 
 /*
+ * pkv_paged_attention_decode_multi with the new tokens' K/V rows appended in the
+ * same launch: position context_lens[s] - num_queries + j of sequence s receives
+ * k_new[s][j], v_new[s][j] in slot block_tables[s][p / B] * B + p % B of both
+ * pools, and the attention uses them for that position.  The result (output and
+ * pools) is that of pkv_slot_mapping over those positions, pkv_kv_cache_write,
+ * then pkv_paged_attention_decode_multi, in one launch instead of three
+ * ("Serving models with vLLM", section "How it works: PagedAttention": the cache
+ * grows block by block as tokens arrive).
+ *   k_new, v_new   [num_seqs][num_queries][num_kv_heads][head_dim], pool type,
+ *                  16-byte aligned
+ *   slot_mapping   optional int64 [num_seqs][num_queries] output: the slot each
+ *                  token went to (-1 for a position outside the context or a bad
+ *                  table entry, which also sets PKV_DEVERR_BLOCK_ID); NULL to skip
+ * The blocks receiving new tokens must belong to their sequence alone (copy them
+ * on write first when shared).  Other arguments as in
+ * pkv_paged_attention_decode_multi.
+ */
+pkv_status pkv_paged_attention_decode_multi_append(
+    const pkv_pool* pool, const void* q, const void* k_new, const void* v_new,
+    int32_t num_queries, int32_t num_seqs, int32_t num_q_heads, const int32_t* block_tables,
+    int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t max_context_len,
+    float scale, void* out, int32_t out_dtype, int32_t partition_size, void* workspace,
+    size_t workspace_bytes, int64_t* slot_mapping, void* stream);
+
+/*
  * Decode for a batch whose sequences all begin with the same prefix_len tokens
  * held in the same physical blocks (a shared system prompt: "Serving models
  * with vLLM", section "How it works: PagedAttention": requests with the same

@@ -408,6 +408,37 @@ pkv_status pkv_paged_attention_decode_multi(
                       static_cast<cudaStream_t>(stream));
 }
 
+pkv_status pkv_paged_attention_decode_multi_append(
+    const pkv_pool* pool, const void* q, const void* k_new, const void* v_new,
+    int32_t num_queries, int32_t num_seqs, int32_t num_q_heads, const int32_t* block_tables,
+    int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t max_context_len,
+    float scale, void* out, int32_t out_dtype, int32_t partition_size, void* workspace,
+    size_t workspace_bytes, int64_t* slot_mapping, void* stream) {
+    if (num_seqs > 0 && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)))
+        return PKV_ERR_INVALID;
+    if (num_queries == 1)
+        return pkv_paged_attention_decode_append(pool, q, k_new, v_new, num_seqs, num_q_heads,
+                                                 block_tables, max_blocks_per_seq, context_lens,
+                                                 max_context_len, scale, out, out_dtype,
+                                                 partition_size, workspace, workspace_bytes,
+                                                 slot_mapping, stream);
+    DecodeArgs a{pool, q, num_seqs, num_q_heads, block_tables, max_blocks_per_seq,
+                 context_lens, max_context_len, scale, partition_size};
+    pkv_status st = check_decode(a);
+    if (st != PKV_OK) return st;
+    if (num_queries < 1 || (int64_t)num_seqs * num_queries > INT32_MAX) return PKV_ERR_INVALID;
+    if (num_seqs > 0 && !out) return PKV_ERR_INVALID;
+    if (out_dtype != PKV_F32 && out_dtype != pool->dtype) return PKV_ERR_UNSUPPORTED;
+    if (pool->dtype == PKV_F32) return PKV_ERR_UNSUPPORTED;
+    a.NQ = num_queries;
+    const int32_t G = num_q_heads / pool->num_kv_heads;
+    if ((int64_t)pool->num_kv_heads * ((num_queries + 8 / G - 1) / (8 / G)) > INT32_MAX)
+        return PKV_ERR_UNSUPPORTED;
+    const AppendArgs app{k_new, v_new, slot_mapping};
+    return run_decode(a, out, out_dtype, 1, workspace, workspace_bytes,
+                      static_cast<cudaStream_t>(stream), &app);
+}
+
 namespace {
 
 struct CascadeShape {

@@ -131,7 +131,76 @@ __device__ __forceinline__ uint32_t swz(int row, int col16) {
 // Columns of the 8-wide N tile: n = (query j - j0) * G + g for the CTA's queries
 // j0 .. j0 + nj - 1 and the G q heads g of kv head kvh.  With one query per
 // sequence (decode) the columns are just the G heads of the group.
-template <typename T, int D, int NW, int NS>
+// Several appended tokens (the last num_queries positions of the context, rows of
+// k_new / v_new [S][NQ][Hkv][D]).  Each warp writes the new rows of its own chunks to
+// their pool slots (append_rows_to_pool) before it issues those chunks' tensor copies,
+// which then bring them; a chunk whose copy was issued earlier (one of the first NS of
+// the warp) gets them put into its staged rows after it lands (append_rows_into_chunk).
+// Compiled only into the kernel variant for several appended tokens per sequence.
+template <typename T, int D>
+__device__ __forceinline__ void append_rows_to_pool(const DecodeParams& p, const int32_t* bt_row,
+                                                    int s, int kvh, int ctx, int t_lo, int t_hi,
+                                                    int lane) {
+    constexpr int VPR = D * 2 / 16;  // 16-byte vectors per row
+    constexpr int RPP = 32 / VPR;    // rows per warp-wide pass
+    constexpr int BATCH = 4;         // passes whose loads are in flight together
+    const int NQ = p.num_queries, Hkv = p.num_kv_heads, B = p.block_size;
+    const int sub = lane / VPR, col = lane % VPR;
+    for (int base = t_lo; base < t_hi; base += RPP * BATCH) {
+        uint4 kr[BATCH], vr[BATCH];
+        int phys[BATCH];
+#pragma unroll
+        for (int b = 0; b < BATCH; ++b) {
+            const int pj = base + b * RPP + sub;
+            phys[b] = -1;
+            if (pj < t_hi) {
+                const size_t src = (((size_t)s * NQ + pj - (ctx - NQ)) * Hkv + kvh) * D;
+                phys[b] = __ldg(bt_row + pj / B);
+                kr[b] = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.k_new) + src) + col);
+                vr[b] = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.v_new) + src) + col);
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < BATCH; ++b) {
+            const int pj = base + b * RPP + sub;
+            if (pj < t_hi && (unsigned)phys[b] < (unsigned)p.num_blocks) {
+                const size_t dst = (((size_t)phys[b] * Hkv + kvh) * B + (pj % B)) * D;
+                reinterpret_cast<uint4*>(const_cast<T*>(static_cast<const T*>(p.k_pool)) + dst)[col] = kr[b];
+                reinterpret_cast<uint4*>(const_cast<T*>(static_cast<const T*>(p.v_pool)) + dst)[col] = vr[b];
+            }
+        }
+    }
+    for (int pj = t_lo + lane; pj < t_hi; pj += 32) {
+        const int ph = __ldg(bt_row + pj / B);
+        const bool ok = (unsigned)ph < (unsigned)p.num_blocks;
+        if (!ok) set_error(p.err, PKV_DEVERR_BLOCK_ID);
+        if (p.slot_out && kvh == 0)
+            p.slot_out[(size_t)s * NQ + pj - (ctx - NQ)] = ok ? (int64_t)ph * B + (pj % B) : -1;
+    }
+}
+
+template <typename T, int D>
+__device__ __forceinline__ void append_rows_into_chunk(const DecodeParams& p, unsigned char* Ks,
+                                                    unsigned char* Vs, int s, int kvh, int ctx,
+                                                    int t_c, int lane) {
+    using Geo = MmaGeometry<D>;
+    constexpr int VPR = D * 2 / 16;
+    constexpr int RPP = 32 / VPR;
+    const int NQ = p.num_queries, Hkv = p.num_kv_heads;
+    const int sub = lane / VPR, col = lane % VPR;
+    const int first = max(ctx - NQ, t_c), last = min(ctx, t_c + CHUNK_TOKENS);
+    const uint32_t ks = smem_addr(Ks), vs = smem_addr(Vs);
+    for (int pj = first + sub; pj < last; pj += RPP) {
+        const size_t src = (((size_t)s * NQ + pj - (ctx - NQ)) * Hkv + kvh) * D + col * 8;
+        const uint32_t o16 = (col / 8) * Geo::BOX_BYTES + swz(pj - t_c, col & 7);
+        cp_async16(ks + o16, static_cast<const T*>(p.k_new) + src);
+        cp_async16(vs + o16, static_cast<const T*>(p.v_new) + src);
+    }
+    cp_async_wait_all();
+    __syncwarp();
+}
+
+template <typename T, int D, int NW, int NS, bool MULTI_APPEND = false>
 __global__ void __launch_bounds__(NW * 32)
 paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
@@ -176,8 +245,12 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int tok0 = skip + part * P;
     if (part > 0 && tok0 >= ctx) return;
     const bool direct = p.direct_single && n_parts <= 1;
-    if ((ctx == 0 || ctx_bad) && p.slot_out && kvh == 0 && part == 0 && threadIdx.x == 0)
-        p.slot_out[s] = -1;
+    // appended tokens (when k_new is set): the last num_queries positions of the context;
+    // the slots of those with no position in it are -1 (one CTA of the sequence writes them)
+    const int NQn = NQ;
+    if (p.slot_out && kvh == 0 && qgrp == 0 && part == 0)
+        for (int j = threadIdx.x; j < NQn; j += NW * 32)
+            if (ctx == 0 || ctx_bad || ctx - NQn + j < 0) p.slot_out[(size_t)s * NQn + j] = -1;
     if (ctx <= skip) {  // nothing to attend to here: zero output or an empty partial
         if (ctx < skip && threadIdx.x == 0 && blockIdx.x == 0) set_error(p.err, PKV_DEVERR_CONTEXT);
         for (int i = threadIdx.x; i < ncols * D; i += NW * 32) {
@@ -230,7 +303,9 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
     // fused append (see decode.cuh)
     const int p_new = ctx - 1;
-    const bool has_new = p.k_new != nullptr && !ctx_bad && p_new >= tok0 && p_new < tok_end;
+    const bool has_new =
+        p.k_new != nullptr && NQn == 1 && !ctx_bad && p_new >= tok0 && p_new < tok_end;
+    const bool multi_new = MULTI_APPEND && p.k_new != nullptr && NQn > 1 && !ctx_bad;
     const int c_new = has_new ? (p_new - tok0) / CHUNK_TOKENS : -1;
     const bool warp_new = has_new && (c_new % NW) == warp;
     constexpr int VPR = D * 2 / 16;  // 16-byte vectors per row
@@ -294,6 +369,20 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
     const int n_pro = n_my < NS ? n_my : NS;
     for (int i = 0; i < n_pro; ++i) issue(i);
+    if constexpr (MULTI_APPEND) {
+        // this warp's new rows into the pool while its first copies fly; the fence and the
+        // warp barrier put them ahead of the copies lane 0 issues from here on
+        if (multi_new && ctx - NQn < tok_end) {
+            const int c_lo = max(ctx - NQn - tok0, 0) / CHUNK_TOKENS;
+            for (int c = c_lo + ((warp - c_lo) % NW + NW) % NW; c < n_chunks; c += NW) {
+                const int t_c = tok0 + c * CHUNK_TOKENS;
+                append_rows_to_pool<T, D>(p, bt_row, s, kvh, ctx, max(ctx - NQn, t_c),
+                                          min(tok_end, t_c + CHUNK_TOKENS), lane);
+            }
+            fence_proxy_async_global();
+            __syncwarp();
+        }
+    }
 
     // ldmatrix row addresses: matrix mi = lane / 8, row lane % 8
     const int mi = lane >> 3, mr = lane & 7;
@@ -326,6 +415,11 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
             if (p.slot_out && kvh == 0 && lane == 0)
                 p.slot_out[s] = ok ? (int64_t)phys_new * B + (p_new % B) : -1;
             __syncwarp();
+        }
+        if constexpr (MULTI_APPEND) {
+            const int t_c = tok0 + c * CHUNK_TOKENS;
+            if (multi_new && i < NS && t_c + CHUNK_TOKENS > ctx - NQn)
+                append_rows_into_chunk<T, D>(p, Ks, Vs, s, kvh, ctx, t_c, lane);
         }
         if (!((bad_stages >> st) & 1)) {
             if (valid < CHUNK_TOKENS) {
@@ -491,8 +585,8 @@ inline bool encode_pool_map(CUtensorMap* map, const void* base, long long rows, 
 
 template <int D> struct MmaShape { static constexpr int NW = 4, NS = (64 * 1024) / (4 * MmaGeometry<D>::STAGE_BYTES); };
 
-template <typename T, int D>
-cudaError_t launch_decode_mma_td(const DecodeParams& p, cudaStream_t stream) {
+template <typename T, int D, bool MULTI_APPEND>
+cudaError_t launch_decode_mma_tdv(const DecodeParams& p, cudaStream_t stream) {
     constexpr int NW = MmaShape<D>::NW, NS = MmaShape<D>::NS;
     constexpr int SMEM = MmaSmem<D, NW, NS>::BYTES;
     static_assert(SMEM <= 227 * 1024, "shared memory");
@@ -501,7 +595,7 @@ cudaError_t launch_decode_mma_td(const DecodeParams& p, cudaStream_t stream) {
     if (rows >= (1ll << 31)) return cudaErrorNotSupported;  // TMA row coordinates are int32
     if (!encode_pool_map<T>(&tk, p.k_pool, rows, D) || !encode_pool_map<T>(&tv, p.v_pool, rows, D))
         return cudaErrorNotSupported;
-    auto kernel = paged_decode_mma_kernel<T, D, NW, NS>;
+    auto kernel = paged_decode_mma_kernel<T, D, NW, NS, MULTI_APPEND>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -515,6 +609,14 @@ cudaError_t launch_decode_mma_td(const DecodeParams& p, cudaStream_t stream) {
     dim3 grid(p.num_kv_heads * groups, p.num_seqs, p.max_parts - p.part_offset);
     kernel<<<grid, NW * 32, SMEM, stream>>>(tk, tv, p);
     return cudaGetLastError();
+}
+
+// the kernel variant appending several tokens per sequence only where it is asked for
+template <typename T, int D>
+cudaError_t launch_decode_mma_td(const DecodeParams& p, cudaStream_t stream) {
+    if (p.k_new != nullptr && p.num_queries > 1)
+        return launch_decode_mma_tdv<T, D, true>(p, stream);
+    return launch_decode_mma_tdv<T, D, false>(p, stream);
 }
 
 template <typename T>

@@ -58,6 +58,9 @@ _SIGS = {
                                                  _f32, _P, _i32, _i32, _P, _sz, _P, _P]),
     "pkv_paged_attention_decode_multi": (_i32, [_PP, _P, _i32, _i32, _i32, _P, _i32, _P, _i32,
                                                 _f32, _P, _i32, _i32, _P, _sz, _P]),
+    "pkv_paged_attention_decode_multi_append": (_i32, [_PP, _P, _P, _P, _i32, _i32, _i32, _P,
+                                                       _i32, _P, _i32, _f32, _P, _i32, _i32, _P,
+                                                       _sz, _P, _P]),
     "pkv_cascade_workspace_bytes": (_sz, [_PP, _i32, _i32, _i32, _i32, _i32]),
     "pkv_paged_attention_decode_cascade": (_i32, [_PP, _P, _i32, _i32, _P, _i32, _P, _i32, _f32,
                                                   _i32, _P, _i32, _i32, _P, _P, _P, _P, _sz, _P]),
@@ -225,6 +228,24 @@ def pkv_paged_attention_decode_multi(q, k_pool, v_pool, block_tables, context_le
         _ptr(context_lens), int(max_context_len), float(scale), _ptr(out), _DTYPE[out.dtype],
         int(partition_size), _ptr(workspace), ws_bytes, _stream(stream, q)),
         "pkv_paged_attention_decode_multi")
+
+
+def pkv_paged_attention_decode_multi_append(q, k_pool, v_pool, k_new, v_new, block_tables,
+                                            context_lens, scale, out, max_context_len,
+                                            partition_size=0, workspace=None, slot_mapping=None,
+                                            stream=None):
+    """q, out: [num_seqs][num_queries][num_q_heads][head_dim]; k_new, v_new:
+    [num_seqs][num_queries][num_kv_heads][head_dim], written to the pools at the last
+    num_queries positions of each context in the same launch."""
+    _contig(q, k_new, v_new, block_tables, context_lens, out, workspace, slot_mapping)
+    pool = make_pool(k_pool, v_pool)
+    S, NQ, Hq, _ = q.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.pkv_paged_attention_decode_multi_append(
+        ctypes.byref(pool), _ptr(q), _ptr(k_new), _ptr(v_new), NQ, S, Hq, _ptr(block_tables),
+        block_tables.shape[1], _ptr(context_lens), int(max_context_len), float(scale), _ptr(out),
+        _DTYPE[out.dtype], int(partition_size), _ptr(workspace), ws_bytes, _ptr(slot_mapping),
+        _stream(stream, q)), "pkv_paged_attention_decode_multi_append")
 
 
 def pkv_cascade_workspace_bytes(k_pool, num_seqs, num_q_heads, max_context_len, prefix_len,

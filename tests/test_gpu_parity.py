@@ -448,6 +448,89 @@ def test_multi_query_decode_matches_oracle(P, dtype, Hq, Hkv, D, B, ctx, nq, psi
     assert_no_device_error(P)
 
 
+@pytest.mark.parametrize("dtype,Hq,Hkv,D,B,ctx,nq,psize", [
+    ("f16", 8, 8, 128, 16, [40, 300, 17, 1500, 4], 4, 0),   # MHA; a context of exactly nq
+    ("bf16", 32, 8, 128, 16, [5, 700, 64, 2000], 3, 512),   # G=4: 2 queries per pass
+    ("bf16", 16, 2, 64, 32, [33, 1025, 3, 0], 2, 256),      # G=8; an empty sequence
+    ("f16", 16, 8, 128, 16, [1, 9, 4096, 31], 8, 1024),     # G=2, 8 queries; ctx < nq
+    ("bf16", 8, 4, 64, 16, [17, 18, 47, 48, 49], 16, 0),    # 16 new rows across block edges
+])
+def test_multi_query_fused_append_equals_write_then_decode(P, dtype, Hq, Hkv, D, B, ctx, nq,
+                                                           psize):
+    w = workloads.build("multiapp", dtype=dtype, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                        block_size=B, context_lens=ctx, seed=43, device=DEV)
+    g = torch.Generator(device=DEV).manual_seed(7)
+    tdt = workloads.TORCH_DTYPE[dtype]
+    S = w.num_seqs
+    q = torch.randn((S, nq, Hq, D), generator=g, device=DEV).to(tdt)
+    kn = torch.randn((S, nq, Hkv, D), generator=g, device=DEV).to(tdt)
+    vn = torch.randn((S, nq, Hkv, D), generator=g, device=DEV).to(tdt)
+    k0, v0 = w.k_pool.clone(), w.v_pool.clone()
+    mcl = w.max_context_len
+    bt, cl = dev_i32(w.block_tables), dev_i32(w.context_lens)
+    ws_bytes = P.pkv_decode_workspace_bytes(w.k_pool, S * nq, Hq, mcl, psize)
+    ws = P.workspace_tensor(ws_bytes, DEV) if ws_bytes else None
+    out = torch.full((S, nq, Hq, D), float("nan"), dtype=torch.float32, device=DEV)
+    slots = torch.full((S, nq), -7, dtype=torch.int64, device=DEV)
+    P.pkv_paged_attention_decode_multi_append(q, w.k_pool, w.v_pool, kn, vn, bt, cl, w.scale,
+                                              out, mcl, psize, ws, slot_mapping=slots)
+    torch.cuda.synchronize()
+    # oracle: the new tokens sit at the last nq positions of each context
+    pos = (w.context_lens[:, None] - nq + np.arange(nq)[None, :]).astype(np.int32)
+    seq = np.repeat(np.arange(S, dtype=np.int32), nq)
+    ref_slots = oracle.slot_mapping(w.block_tables, pos.reshape(-1), B, token_seq=seq)
+    assert np.array_equal(slots.cpu().numpy().reshape(-1), ref_slots)
+    kr, vr = host(k0).copy(), host(v0).copy()
+    oracle.kv_cache_write(dtype, kr, vr, host(kn).reshape(S * nq, Hkv, D),
+                          host(vn).reshape(S * nq, Hkv, D), ref_slots)
+    assert np.array_equal(host(w.k_pool), kr) and np.array_equal(host(w.v_pool), vr)
+    ref = oracle.paged_decode_multi(dtype, kr, vr, host(q), w.block_tables, w.context_lens,
+                                    w.scale)
+    live = (pos >= 0)
+    assert not np.isnan(host(out)[~live]).any()             # rows that see nothing are written too
+    assert max_abs(out, ref) <= TOL[dtype]
+    # bit-identical to slot mapping + cache write + multi-query decode on the GPU
+    k2, v2 = k0.clone(), v0.clone()
+    s2 = torch.empty(S * nq, dtype=torch.int64, device=DEV)
+    P.pkv_slot_mapping(bt, dev_i32(pos.reshape(-1)), B, s2, token_seq=dev_i32(seq))
+    P.pkv_kv_cache_write(k2, v2, kn.reshape(S * nq, Hkv, D), vn.reshape(S * nq, Hkv, D), s2)
+    out2 = torch.full_like(out, float("nan"))
+    P.pkv_paged_attention_decode_multi(q, k2, v2, bt, cl, w.scale, out2, mcl, psize, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(k2, w.k_pool) and torch.equal(v2, w.v_pool)
+    assert torch.equal(out, out2)
+    assert_no_device_error(P)
+
+
+def test_multi_query_fused_append_flags_a_bad_table_entry(P):
+    w = workloads.build("multiapp_bad", dtype="f16", num_q_heads=8, num_kv_heads=8, head_dim=128,
+                        block_size=16, context_lens=[40, 100], seed=44, device=DEV)
+    nq = 4
+    bt = w.block_tables.copy()
+    bt[1, (100 - 1) // 16] = -1                         # the block the new rows of seq 1 land in
+    g = torch.Generator(device=DEV).manual_seed(8)
+    q = torch.randn((2, nq, 8, 128), generator=g, device=DEV).half()
+    kn = torch.randn((2, nq, 8, 128), generator=g, device=DEV).half()
+    vn = torch.randn_like(kn)
+    k0 = w.k_pool.clone()
+    out = torch.zeros((2, nq, 8, 128), dtype=torch.float32, device=DEV)
+    slots = torch.full((2, nq), -7, dtype=torch.int64, device=DEV)
+    P.pkv_paged_attention_decode_multi_append(q, w.k_pool, w.v_pool, kn, vn, dev_i32(bt),
+                                              dev_i32(w.context_lens), w.scale, out, 100, 0,
+                                              None, slot_mapping=slots)
+    torch.cuda.synchronize()
+    s = slots.cpu().numpy()
+    assert np.all(s[1] == -1) and np.all(s[0] >= 0)
+    err = P.pkv_get_device_error()
+    assert err & P.DEVERR["BLOCK_ID"]
+    # the first sequence's rows went in; nothing was written through the bad entry
+    k_expect = host(k0).copy()
+    for j in range(nq):
+        sl = int(s[0, j])
+        k_expect[sl // 16, :, sl % 16, :] = host(kn)[0, j]
+    assert np.array_equal(host(w.k_pool), k_expect)
+
+
 # ------------------------------------------------------------------ exactly what bench.py times
 
 def _assert_16bit_close(got, ref, dtype):
