@@ -67,6 +67,24 @@ def test_decode_argument_checks(P):
     assert _decode(P, _pool(), ptrs=False) == P.PKV_ERR_INVALID
     assert _decode(P, _pool(), max_ctx=5000, P_=512) == P.PKV_ERR_WORKSPACE
     assert _decode(P, _pool(), S=0) == P.PKV_OK                      # nothing to do
+    assert _decode(P, _pool(), S=65536) == P.PKV_ERR_UNSUPPORTED     # one grid row per sequence
+
+
+def test_multi_query_append_argument_checks(P):
+    d = ctypes.c_void_p(256)
+
+    def call(pool, kn=d, vn=d, nq=4, S=1, out_dtype=1):
+        return P.lib.pkv_paged_attention_decode_multi_append(
+            ctypes.byref(pool), d, kn, vn, nq, S, 2, d, 4, d, 10, 0.1, d, out_dtype, 0, None, 0,
+            None, None)
+
+    assert call(_pool(), kn=None) == P.PKV_ERR_INVALID
+    assert call(_pool(), vn=ctypes.c_void_p(8)) == P.PKV_ERR_INVALID      # misaligned rows
+    assert call(_pool(), nq=0) == P.PKV_ERR_INVALID
+    assert call(_pool(dtype=0), out_dtype=0) == P.PKV_ERR_UNSUPPORTED     # fp32 pool
+    assert call(_pool(), out_dtype=2) == P.PKV_ERR_UNSUPPORTED            # bf16 out, fp16 pool
+    assert call(_pool(), S=65536) == P.PKV_ERR_UNSUPPORTED
+    assert call(_pool(), S=0) == P.PKV_OK
 
 
 def test_workspace_sizes(P):

@@ -236,6 +236,22 @@ def test_copy_blocks_bit_exact_and_cow_is_a_no_op(P):
     assert_no_device_error(P)
 
 
+# ------------------------------------------------------------------ the largest batch the grid takes
+
+@pytest.mark.parametrize("engine", [1, 2], ids=["cuda_cores", "tensor_cores"], indirect=True)
+@pytest.mark.parametrize("psize", [0, 16])
+def test_largest_batch_the_grid_takes(P, engine, psize):
+    """65535 sequences (one grid row each; one more is refused on the host), ragged contexts
+    of 0-40 tokens; with partitions of one block most rows go through the merge."""
+    ctx = np.random.default_rng(71).integers(0, 41, size=65535)
+    w = workloads.build("maxgrid", dtype="bf16", num_q_heads=4, num_kv_heads=2, head_dim=64,
+                        block_size=16, context_lens=ctx, seed=71, device=DEV)
+    out = run_decode(P, w, partition_size=psize)
+    assert max_abs(out, oracle_decode(w)) <= TOL["bf16"]
+    assert torch.all(out[torch.as_tensor(ctx == 0, device=DEV)] == 0)
+    assert_no_device_error(P)
+
+
 # ------------------------------------------------------------------ device-side error reporting
 
 def test_bad_block_id_sets_flag_without_faulting(P):
