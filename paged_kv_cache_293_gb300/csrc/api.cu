@@ -536,29 +536,11 @@ pkv_status pkv_paged_attention_decode_cascade(
     float* ws_l = reinterpret_cast<float*>(ws + lay.l_off);
     float* ws_o = reinterpret_cast<float*>(ws + lay.o_off);
     const int G = num_q_heads / pool->num_kv_heads;
-
-    pkv::PrefixParams pp{};
-    pp.q = q;
-    pp.num_seqs = num_seqs;
-    pp.num_q_heads = num_q_heads;
-    pp.num_kv_heads = pool->num_kv_heads;
-    pp.num_blocks = pool->num_blocks;
-    pp.block_size = pool->block_size;
-    pp.block_tables = block_tables;
-    pp.max_blocks_per_seq = max_blocks_per_seq;
-    pp.prefix_len = prefix_len;
-    pp.scale_log2 = scale * 1.4426950408889634f;
-    pp.max_parts = c.max_parts;
-    pp.tokens_per_split = c.tokens_per_split;
-    pp.ws_m = ws_m;
-    pp.ws_l = ws_l;
-    pp.ws_o = ws_o;
-    pp.err = err;
-    cudaError_t e = pool->dtype == PKV_F16
-                        ? pkv::launch_prefix<__half>(pp, pool->k, pool->v, pool->head_dim, s)
-                        : pkv::launch_prefix<__nv_bfloat16>(pp, pool->k, pool->v, pool->head_dim, s);
-    if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
-    if (e != cudaSuccess) return PKV_ERR_CUDA;
+    // the prefix pass's limits (tensor-map rows, 128-row tiles in grid.y), checked before
+    // anything is launched
+    if ((int64_t)pool->num_blocks * pool->num_kv_heads * pool->block_size >= (1ll << 31) ||
+        ((int64_t)num_seqs * G + 127) / 128 > 65535)
+        return PKV_ERR_UNSUPPORTED;
 
     pkv::DecodeParams p{};
     p.k_pool = pool->k;
@@ -590,9 +572,35 @@ pkv_status pkv_paged_attention_decode_cascade(
     p.v_new = v_new;
     p.slot_out = slot_mapping;
     p.err = err;
-    // the suffix decode's grid covers max_parts - part_offset = suffix partitions
+    // the suffix decode's grid covers max_parts - part_offset = suffix partitions.  It goes
+    // first and lets the prefix pass start on the SMs its last CTAs leave idle (the two
+    // read and write disjoint data); the prefix pass ends only after it.
+    p.trigger_dependents = 1;
     if (launch_decode_typed(p, pool->dtype, pool->head_dim, G, s) != cudaSuccess)
         return PKV_ERR_CUDA;
+
+    pkv::PrefixParams pp{};
+    pp.q = q;
+    pp.num_seqs = num_seqs;
+    pp.num_q_heads = num_q_heads;
+    pp.num_kv_heads = pool->num_kv_heads;
+    pp.num_blocks = pool->num_blocks;
+    pp.block_size = pool->block_size;
+    pp.block_tables = block_tables;
+    pp.max_blocks_per_seq = max_blocks_per_seq;
+    pp.prefix_len = prefix_len;
+    pp.scale_log2 = scale * 1.4426950408889634f;
+    pp.max_parts = c.max_parts;
+    pp.tokens_per_split = c.tokens_per_split;
+    pp.ws_m = ws_m;
+    pp.ws_l = ws_l;
+    pp.ws_o = ws_o;
+    pp.err = err;
+    cudaError_t e = pool->dtype == PKV_F16
+                        ? pkv::launch_prefix<__half>(pp, pool->k, pool->v, pool->head_dim, s)
+                        : pkv::launch_prefix<__nv_bfloat16>(pp, pool->k, pool->v, pool->head_dim, s);
+    if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
 
     pkv::MergeParams mp{};
     mp.ws_m = ws_m;

@@ -213,6 +213,7 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
+    if (p.trigger_dependents) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int Hkv = p.num_kv_heads;
     const int kvh = blockIdx.x % Hkv, qgrp = blockIdx.x / Hkv, s = blockIdx.y, part = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

@@ -53,6 +53,10 @@ struct DecodeParams {
     const void* v_new;
     int64_t* slot_out;      // optional: the slot each new token went to (-1: none)
     unsigned int* err;
+    // tensor-core kernel, 1: every CTA lets the next launch in the stream (programmatic
+    // dependent launch) begin as soon as it starts, so that launch fills the SMs this
+    // grid's last CTAs leave idle; it must not read what this grid writes
+    int32_t trigger_dependents;
 };
 
 struct MergeParams {

@@ -459,6 +459,9 @@ prefix_attention_kernel(const __grid_constant__ CUtensorMap tmap_k,
         umma::fence_after_sync();
         umma::dealloc(tmem, L::TMEM_COLS);
     }
+    // launched early behind the suffix decode (programmatic dependent launch): finish only
+    // after it, so that the merge launched behind this grid sees both grids' partials
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <typename T, int D>
@@ -487,8 +490,20 @@ cudaError_t launch_prefix_td(const PrefixParams& p, const void* k_pool, const vo
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    kernel<<<grid, PREFIX_THREADS, SMEM, stream>>>(tk, tv, p);
-    return cudaGetLastError();
+    // programmatic dependent launch: the CTAs may start while the grid before this one in
+    // the stream (the suffix decode, which triggers at its start) still runs; nothing here
+    // reads what that grid writes
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(PREFIX_THREADS);
+    cfg.dynamicSmemBytes = SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, tk, tv, p);
 }
 
 template <typename T>
