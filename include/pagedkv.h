@@ -242,11 +242,12 @@ pkv_status pkv_paged_attention_decode_multi_append(
  * with vLLM", section "How it works: PagedAttention": requests with the same
  * prefix point at the same physical blocks).  Same result as
  * pkv_paged_attention_decode (or, with k_new / v_new, as
- * pkv_paged_attention_decode_append), computed in three launches: attention of
- * all sequences' queries over the shared prefix, read once per kv head and run
- * on tensor cores; the paged decode of each sequence's own positions
- * [prefix_len, context_lens[s]) in partitions of partition_size (0 =
- * automatic); and the log-sum-exp merge of the two.
+ * pkv_paged_attention_decode_append), computed in three launches: the paged
+ * decode of each sequence's own positions [prefix_len, context_lens[s]) in
+ * partitions of partition_size (0 = automatic); the attention of all sequences'
+ * queries over the shared prefix, read once per kv head and run on tensor cores
+ * (launched so that it may start on the SMs the first launch's last CTAs leave
+ * idle); and the log-sum-exp merge of the two.
  *   prefix_len   > 0, a multiple of 16 and of block_size, <= every context length;
  *                the first prefix_len / B table entries of every sequence must equal
  *                sequence 0's (checked on the device: PKV_DEVERR_PREFIX)
@@ -255,7 +256,10 @@ pkv_status pkv_paged_attention_decode_multi_append(
  *                lie past the prefix) as the fused entry point does; NULL for none
  *   slot_mapping optional output as in pkv_paged_attention_decode_append
  *   workspace    pkv_cascade_workspace_bytes(...) bytes, always required
- * fp16 / bf16 pools only (PKV_ERR_UNSUPPORTED for fp32).
+ * fp16 / bf16 pools only (PKV_ERR_UNSUPPORTED for fp32).  PKV_ERR_UNSUPPORTED also
+ * for a pool of 2^31 or more (block, kv head, position) rows or more than
+ * 65535 x 128 query rows (num_seqs x group size); every such error is returned
+ * before anything is launched.
  */
 size_t pkv_cascade_workspace_bytes(const pkv_pool* pool, int32_t num_seqs, int32_t num_q_heads,
                                    int32_t max_context_len, int32_t prefix_len,

@@ -526,6 +526,11 @@ pkv_status pkv_paged_attention_decode_cascade(
     if (c.suffix_parts > 65535) return PKV_ERR_UNSUPPORTED;
     const WsLayout lay = ws_layout(num_seqs, num_q_heads, pool->head_dim, c.max_parts);
     if (!workspace || !aligned16(workspace) || workspace_bytes < lay.bytes) return PKV_ERR_WORKSPACE;
+    // the prefix pass's limits (tensor-map rows, 128-row tiles in grid.y), checked before
+    // anything is launched
+    if ((int64_t)pool->num_blocks * pool->num_kv_heads * pool->block_size >= (1ll << 31) ||
+        ((int64_t)num_seqs * (num_q_heads / pool->num_kv_heads) + 127) / 128 > 65535)
+        return PKV_ERR_UNSUPPORTED;
     if (num_seqs == 0) return PKV_OK;
     unsigned int* err = nullptr;
     st = error_word(&err);
@@ -536,11 +541,6 @@ pkv_status pkv_paged_attention_decode_cascade(
     float* ws_l = reinterpret_cast<float*>(ws + lay.l_off);
     float* ws_o = reinterpret_cast<float*>(ws + lay.o_off);
     const int G = num_q_heads / pool->num_kv_heads;
-    // the prefix pass's limits (tensor-map rows, 128-row tiles in grid.y), checked before
-    // anything is launched
-    if ((int64_t)pool->num_blocks * pool->num_kv_heads * pool->block_size >= (1ll << 31) ||
-        ((int64_t)num_seqs * G + 127) / 128 > 65535)
-        return PKV_ERR_UNSUPPORTED;
 
     pkv::DecodeParams p{};
     p.k_pool = pool->k;

@@ -70,6 +70,28 @@ def test_decode_argument_checks(P):
     assert _decode(P, _pool(), S=65536) == P.PKV_ERR_UNSUPPORTED     # one grid row per sequence
 
 
+def test_cascade_argument_checks(P):
+    d = ctypes.c_void_p(256)
+
+    def call(pool, prefix=32, max_ctx=100, kn=None, vn=None, ws=d, ws_bytes=1 << 30, S=2):
+        return P.lib.pkv_paged_attention_decode_cascade(
+            ctypes.byref(pool), d, S, 2, d, 16, d, max_ctx, 0.1, prefix, d, 0, 0, kn, vn, None,
+            ws, ws_bytes, None)
+
+    assert call(_pool(dtype=0)) == P.PKV_ERR_UNSUPPORTED                  # fp32 pool
+    assert call(_pool(), prefix=24) == P.PKV_ERR_INVALID                  # not a multiple of 16
+    assert call(_pool(), prefix=0) == P.PKV_ERR_INVALID
+    assert call(_pool(), prefix=112) == P.PKV_ERR_INVALID                 # past max_context_len
+    assert call(_pool(), kn=d) == P.PKV_ERR_INVALID                       # k_new without v_new
+    assert call(_pool(), ws=None) == P.PKV_ERR_WORKSPACE
+    assert call(_pool(), ws_bytes=16) == P.PKV_ERR_WORKSPACE
+    # 2^32 (block, kv head, position) rows: past the tensor maps' int32 rows, refused
+    # before any launch
+    assert call(_pool(num_blocks=1 << 27)) == P.PKV_ERR_UNSUPPORTED
+    f = P.lib.pkv_cascade_workspace_bytes
+    assert f(ctypes.byref(_pool()), 2, 2, 100, 32, 0) > 0
+
+
 def test_multi_query_append_argument_checks(P):
     d = ctypes.c_void_p(256)
 
