@@ -428,37 +428,48 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
 
 
-def run_e2e(P, w, st, args, device, pools):
-    """The same step end to end through the binding: every step copies its inputs (q, new
-    K/V rows, block tables, positions, lengths) from pinned host memory and reads its output
-    back.  As a serving loop would, the copies run on their own stream two steps deep: step
-    i+1's inputs go in while step i computes, and step i's output comes back while step i+1
-    computes.  Consecutive steps read two different KV pools of the batch's shape (two
-    layers' caches, each larger than L2), so no step finds the previous step's pages in L2.
-    Timed with CUDA events from the first input copy to the last output copy."""
-    names = ["q", "k_new", "v_new", "bt", "pos", "ctx"]
-    dev_src = {"q": w.q, "k_new": w.k_new, "v_new": w.v_new, "bt": st.bt, "pos": st.pos,
-               "ctx": st.ctx}
-    host_in = {k: v.detach().cpu().pin_memory() for k, v in dev_src.items()}
-    bufs = [{k: torch.empty_like(v) for k, v in dev_src.items()} for _ in range(2)]
-    outs = [torch.empty_like(st.out) for _ in range(2)]
-    h_out = [torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory() for _ in range(2)]
-    h2d = sum(h.numel() * h.element_size() for h in host_in.values())
+def _e2e_two_deep(device, dev_src, out_like, step, warmup, steps):
+    """End-to-end timing through the binding: every step copies its inputs (`dev_src`, a
+    dict of device tensors whose pinned host copy is made here) in from pinned host memory,
+    in one copy, and reads its output back.  As a serving loop would, the copies run on their own
+    stream two steps deep: step i+1's inputs go in while step i computes, and step i's output
+    comes back while step i+1 computes.  `step(inputs, out, slot)` launches one step on the
+    current stream, reading `inputs` (a dict like `dev_src`) and writing `out`; `slot` (0 or
+    1) alternates between steps.  Timed with CUDA events from the first input copy to the
+    last output copy; returns ms per step and the bytes copied each way per step."""
+    # the inputs packed into one pinned buffer (each at a 256-byte offset), so a step's
+    # inputs go in by one copy, as a serving loop that stages them would send them
+    offs, total = {}, 0
+    for k, v in dev_src.items():
+        offs[k] = total
+        total += (v.numel() * v.element_size() + 255) // 256 * 256
+    host_in = torch.zeros(total, dtype=torch.uint8).pin_memory()
+    for k, v in dev_src.items():
+        n = v.numel() * v.element_size()
+        host_in[offs[k]:offs[k] + n].copy_(v.detach().contiguous().view(-1).view(torch.uint8).cpu())
+    dev_in = [torch.empty(total, dtype=torch.uint8, device=device) for _ in range(2)]
+
+    def views(buf):
+        return {k: buf[offs[k]:offs[k] + v.numel() * v.element_size()].view(v.dtype).view(v.shape)
+                for k, v in dev_src.items()}
+
+    bufs = [views(d) for d in dev_in]
+    outs = [torch.empty_like(out_like) for _ in range(2)]
+    h_out = [torch.empty(out_like.shape, dtype=out_like.dtype).pin_memory() for _ in range(2)]
+    h2d = total
     d2h = h_out[0].numel() * h_out[0].element_size()
     comp = torch.cuda.current_stream(device)
     copy = torch.cuda.Stream(device)
     in_ready = [torch.cuda.Event() for _ in range(2)]
     computed = [torch.cuda.Event() for _ in range(2)]
     out_read = [torch.cuda.Event() for _ in range(2)]
-    saved = (w.q, w.k_new, w.v_new, st.bt, st.pos, st.ctx, st.out, w.k_pool, w.v_pool)
 
     def load(i):
         b = i % 2
         if i >= 2:
             copy.wait_event(computed[b])        # step i - 2 is done with this buffer
         with torch.cuda.stream(copy):
-            for k in names:
-                bufs[b][k].copy_(host_in[k], non_blocking=True)
+            dev_in[b].copy_(host_in, non_blocking=True)
         in_ready[b].record(copy)
 
     def run(n):
@@ -474,11 +485,7 @@ def run_e2e(P, w, st, args, device, pools):
             comp.wait_event(in_ready[b])
             if i >= 2:
                 comp.wait_event(out_read[b])    # step i - 2's output has been read back
-            w.q, w.k_new, w.v_new = bufs[b]["q"], bufs[b]["k_new"], bufs[b]["v_new"]
-            st.bt, st.pos, st.ctx, st.out = bufs[b]["bt"], bufs[b]["pos"], bufs[b]["ctx"], outs[b]
-            w.k_pool, w.v_pool = pools[b]
-            st.pre_decode()
-            st.decode()
+            step(bufs[b], outs[b], b)
             computed[b].record(comp)
             copy.wait_event(computed[b])
             with torch.cuda.stream(copy):
@@ -488,12 +495,30 @@ def run_e2e(P, w, st, args, device, pools):
         t1.synchronize()
         return t0.elapsed_time(t1) / n
 
+    run(max(3, warmup))
+    return {"ms": run(max(3, steps)), "h2d": h2d, "d2h": d2h}
+
+
+def run_e2e(P, w, st, args, device, pools):
+    """The decode step end to end: q, the new K/V rows, block tables, positions and lengths
+    in from pinned host memory every step, the output back, two steps deep; consecutive
+    steps read two different KV pools of the batch's shape (two layers' caches, each larger
+    than L2), so no step finds the previous step's pages in L2."""
+    dev_src = {"q": w.q, "k_new": w.k_new, "v_new": w.v_new, "bt": st.bt, "pos": st.pos,
+               "ctx": st.ctx}
+    saved = (w.q, w.k_new, w.v_new, st.bt, st.pos, st.ctx, st.out, w.k_pool, w.v_pool)
+
+    def step(x, out, b):
+        w.q, w.k_new, w.v_new = x["q"], x["k_new"], x["v_new"]
+        st.bt, st.pos, st.ctx, st.out = x["bt"], x["pos"], x["ctx"], out
+        w.k_pool, w.v_pool = pools[b]
+        st.pre_decode()
+        st.decode()
+
     try:
-        run(max(3, args.warmup))
-        ms = run(max(3, args.steps // 4))
+        return _e2e_two_deep(device, dev_src, st.out, step, args.warmup, args.steps // 4)
     finally:
         w.q, w.k_new, w.v_new, st.bt, st.pos, st.ctx, st.out, w.k_pool, w.v_pool = saved
-    return {"ms": ms, "h2d": h2d, "d2h": d2h}
 
 
 def run_reference(args):
@@ -621,17 +646,23 @@ def run_multi(args):
     def prepare(i):
         cur["k"], cur["v"] = pools[i % 2]
 
-    def body_unfused():
-        P.pkv_slot_mapping(bt, pos, w.block_size, slots, token_seq=tseq)
-        P.pkv_kv_cache_write(cur["k"], cur["v"], k_new, v_new, slots)
-        P.pkv_paged_attention_decode_multi(q, cur["k"], cur["v"], bt, ctx, w.scale, out, mcl, 0,
-                                           ws)
+    dev_in = {"q": q, "k_new": k_new, "v_new": v_new, "bt": bt, "ctx": ctx}
+    if args.unfused:   # the fused launch derives the positions from the lengths
+        dev_in.update(pos=pos, tseq=tseq)
 
-    def body_fused():
-        P.pkv_paged_attention_decode_multi_append(q, cur["k"], cur["v"], k_new, v_new, bt, ctx,
-                                                  w.scale, out, mcl, 0, ws, slot_mapping=slots)
+    def launch(x, o, kp, vp):
+        if args.unfused:
+            P.pkv_slot_mapping(x["bt"], x["pos"], w.block_size, slots, token_seq=x["tseq"])
+            P.pkv_kv_cache_write(kp, vp, x["k_new"], x["v_new"], slots)
+            P.pkv_paged_attention_decode_multi(x["q"], kp, vp, x["bt"], x["ctx"], w.scale, o, mcl,
+                                               0, ws)
+        else:
+            P.pkv_paged_attention_decode_multi_append(x["q"], kp, vp, x["k_new"], x["v_new"],
+                                                      x["bt"], x["ctx"], w.scale, o, mcl, 0, ws,
+                                                      slot_mapping=slots)
 
-    body = body_unfused if args.unfused else body_fused
+    def body():
+        launch(dev_in, out, cur["k"], cur["v"])
 
     stream = torch.cuda.current_stream(device)
     ms, clocks = _time_steps(device, stream, args.steps, args.warmup, prepare, body)
@@ -645,20 +676,12 @@ def run_multi(args):
     total = kv + qo + table + write    # partition partials not counted
     peak, peak_kind = read_peaks()
 
-    # the same step end to end: q and the new rows in from pinned host memory, out back
-    h_in = [t.cpu().pin_memory() for t in (q, k_new, v_new)]
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    d_in = (q, k_new, v_new)
-
-    def e2e_body():
-        for d, h in zip(d_in, h_in):
-            d.copy_(h, non_blocking=True)
-        body()
-        h_out.copy_(out, non_blocking=True)
-
-    e2e_ms, _ = _time_steps(device, stream, max(3, args.steps // 4), 3, prepare, e2e_body)
-    h2d = sum(h.numel() * h.element_size() for h in h_in)
-    d2h = h_out.numel() * h_out.element_size()
+    # the same step end to end: q, the new rows, tables, lengths and positions in from
+    # pinned host memory every step, out back, two steps deep
+    e2e = _e2e_two_deep(device, dev_in, out,
+                        lambda x, o, b: launch(x, o, pools[b][0], pools[b][1]),
+                        args.warmup, args.steps // 4)
+    e2e_ms, h2d, d2h = e2e["ms"], e2e["h2d"], e2e["d2h"]
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -700,7 +723,8 @@ def run_multi(args):
          "traffic": None, "algorithmic_bytes": total},
         cpu,
         {"value": round(total / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-         "ms_per_step": round(e2e_ms, 5), "overlap": "none: copies, step and read-back in order",
+         "ms_per_step": round(e2e_ms, 5),
+         "overlap": "input and output copies on their own stream, two steps deep",
          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         ((3 if args.unfused else 1) + (1 if ws_bytes else 0)) * args.steps, clocks)
     line["tokens_per_s_per_layer"] = round(S * nq / (ms * 1e-3), 1)
