@@ -14,10 +14,10 @@
 //
 // CTA = 128 query rows of one kv head (the MMA's M) x one split of the prefix,
 // taken in chunks of 64 tokens.  Eleven warps with fixed roles:
-//   warps 8 and 10, one lane each: TMA tensor copies of each chunk's K pages
-//     (warp 8) and V pages (warp 10) -- 128-byte swizzle, 16-token boxes -- into a
-//     six-stage K ring and a five-stage V ring; a K stage is released as soon as
-//     its Q.K^T is done, a V stage after its P.V;
+//   warps 8 and 10: TMA tensor copies of each chunk's K pages (warp 8) and V pages
+//     (warp 10) -- 128-byte swizzle, 16-token boxes -- into a two-stage K ring and a
+//     two-stage V ring (two CTAs per SM); a K stage is released as soon as its
+//     Q.K^T is done, a V stage after its P.V;
 //   warp 9, one lane: issues the MMAs --
 //     S_j [128 rows x 64 tokens] = Q . K_j^T   (tensor memory, two buffers)
 //     O   [128 rows x D]        += P_j . V_j   (tensor memory; P_j is written over
@@ -26,7 +26,8 @@
 //     and learns of their completion through tcgen05.commit on mbarriers;
 //   warps 0-7: the softmax.  Warp w reads lanes 32 (w % 4) .. + 31 (its rows) and
 //     half w / 4 of each S tile's columns; the two warps of a row quarter agree on
-//     the row's chunk maximum through shared memory.
+//     the row's chunk maximum (and at the end its sum) through shared memory; at the
+//     end they write O as whole rows, staged through the then idle Q tile and rings.
 // The running maximum is kept lazily: P = 2^(s - m_ref) with the reference m_ref
 // raised only when a chunk's maximum exceeds it by more than 8 (base-2 units), so
 // the O accumulator in tensor memory is rescaled (read, scaled and written back
@@ -409,11 +410,14 @@ prefix_attention_kernel(const __grid_constant__ CUtensorMap tmap_k,
             ok = __all_sync(FULL_MASK, mbar_wait(o_done, 0));
             if (ok) l += exchange(n_chunks, l);
         }
-        // O leaves through shared memory (the K ring, idle once every MMA is done) so
-        // that each warp then writes whole rows: row r of the staging area holds D floats
-        // at a stride of D + 4 (no bank conflicts between the rows of a warp's store).
-        float* stage = reinterpret_cast<float*>(smem + L::K_OFF);
+        // O leaves through shared memory so that each warp then writes whole rows: row r
+        // of the staging area holds D floats at a stride of D + 4 (no bank conflicts
+        // between the rows of a warp's store).  The area spans the Q tile and the K and V
+        // rings, all idle once every MMA is done, and ends before the exchange area, which
+        // the other warp of a row quarter may still be reading.
         constexpr int SROW = D + 4;
+        static_assert(L::Q_OFF + PREFIX_ROWS * SROW * 4 <= L::RED_OFF, "O staging area");
+        float* stage = reinterpret_cast<float*>(smem + L::Q_OFF);
         if (ok && n_chunks > 0) {
             umma::fence_after_sync();
 #pragma unroll

@@ -611,6 +611,34 @@ def test_bench_step_matches_oracle_at_full_size(P, name):
 
 # ------------------------------------------------------------------ shared-prefix (cascade) decode
 
+def test_cascade_step_is_deterministic(P):
+    """The cascade's three launches overlap (the prefix pass starts while the suffix decode's
+    last CTAs run), and every floating-point result depends only on the inputs: repeated
+    steps on the full shared-prefix GQA batch give bit-identical output and partials.  (A
+    prefix-pass CTA that staged its output over the area where its warps exchange row sums
+    once showed up here as 4-8 rows differing in about one step in three.)"""
+    import bench
+    w = workloads.make("gqa_prefix", seed=0, device=DEV)
+    k0, v0 = w.k_pool.clone(), w.v_pool.clone()
+    st = bench.Step(P, w, torch.device(DEV), fused=True, cascade=True)
+    assert st.prefix_len > 0
+    first = None
+    for _ in range(8):
+        w.k_pool.copy_(k0)
+        w.v_pool.copy_(v0)
+        st.ws.zero_()
+        st.pre_decode()
+        st.decode()
+        torch.cuda.synchronize()
+        got = (st.out.clone(), st.ws.clone())
+        if first is None:
+            first = got
+        else:
+            assert torch.equal(got[0], first[0]) and torch.equal(got[1], first[1])
+    assert_no_device_error(P)
+
+
+
 @pytest.mark.parametrize("dtype,Hq,Hkv,D,B,prefix_blocks,suffix,psize", [
     ("bf16", 32, 8, 128, 16, 4, [1, 30, 700, 2000, 16], 0),     # tensor-core suffix, G = 4
     ("f16", 8, 8, 128, 32, 3, [5, 64, 1100, 33], 512),         # CUDA-core suffix (MHA), B = 32
