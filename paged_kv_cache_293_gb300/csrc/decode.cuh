@@ -77,6 +77,8 @@ __global__ void __launch_bounds__(NW * 32)
 paged_decode_kernel(const DecodeParams p) {
     using Geo = Geometry<T, D>;
     using Smem = DecodeSmem<T, D, NW, NS>;
+    // the warps' partial results are combined over the ring, which must hold them
+    static_assert(NW * G * (D + 2) * 4 <= Smem::RING_BYTES, "combination area");
     constexpr int CPR = Geo::CPR, RPP = Geo::RPP, PASSES = Geo::PASSES, PV = Geo::PER_VEC;
     constexpr int ROWB = Geo::ROW_BYTES, CHB = Geo::CHUNK_BYTES;
 
