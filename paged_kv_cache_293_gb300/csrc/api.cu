@@ -19,17 +19,19 @@ namespace {
 __device__ unsigned int g_error_word;
 
 constexpr int MAX_DEVICES = 64;
-unsigned int* g_error_ptr[MAX_DEVICES] = {nullptr};
+std::atomic<unsigned int*> g_error_ptr[MAX_DEVICES];  // looked up once per device
 
 pkv_status error_word(unsigned int** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return PKV_ERR_CUDA;
-    if (!g_error_ptr[dev]) {
+    unsigned int* w = g_error_ptr[dev].load(std::memory_order_acquire);
+    if (!w) {  // callers racing here all find the same address
         void* ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_error_word) != cudaSuccess) return PKV_ERR_CUDA;
-        g_error_ptr[dev] = static_cast<unsigned int*>(ptr);
+        w = static_cast<unsigned int*>(ptr);
+        g_error_ptr[dev].store(w, std::memory_order_release);
     }
-    *out = g_error_ptr[dev];
+    *out = w;
     return PKV_OK;
 }
 
@@ -447,19 +449,19 @@ struct CascadeShape {
 
 // Streaming multiprocessors of the current device (152 when it cannot be asked).
 int32_t sm_count() {
-    static int32_t cached[64] = {0};
+    static std::atomic<int32_t> cached[64];  // 0 until asked; racing callers agree
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
-    if (cached[dev] == 0) {
-        int n = 0;
+    int32_t n = cached[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
             n = 152;
-        cached[dev] = n;
+        cached[dev].store(n, std::memory_order_relaxed);
     }
-    return cached[dev];
+    return n;
 }
 
-// The prefix pass runs one CTA per SM over (kv head, 128-row tile, split of the
+// The prefix pass runs two CTAs per SM over (kv head, 128-row tile, split of the
 // prefix); the split count minimises waves x (64-token chunks per split + 3), the 3
 // standing for a CTA's fixed cost (query tile, pipeline fill, epilogue).  Each split
 // writes one slot, followed by the suffix partitions.

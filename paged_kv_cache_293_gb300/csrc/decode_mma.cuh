@@ -600,11 +600,11 @@ cudaError_t launch_decode_mma_tdv(const DecodeParams& p, cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    static bool configured[64] = {false};
-    if (dev < 64 && !configured[dev]) {
+    static std::atomic<bool> configured[64];  // per device; setting it twice is harmless
+    if (dev < 64 && !configured[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
         if (e != cudaSuccess) return e;
-        configured[dev] = true;
+        configured[dev].store(true, std::memory_order_release);
     }
     const int groups = (p.num_queries + p.queries_per_cta - 1) / p.queries_per_cta;
     dim3 grid(p.num_kv_heads * groups, p.num_seqs, p.max_parts - p.part_offset);

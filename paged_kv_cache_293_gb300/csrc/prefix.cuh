@@ -488,11 +488,11 @@ cudaError_t launch_prefix_td(const PrefixParams& p, const void* k_pool, const vo
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    static bool configured[64] = {false};
-    if (dev < 64 && !configured[dev]) {
+    static std::atomic<bool> configured[64];  // per device; setting it twice is harmless
+    if (dev < 64 && !configured[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
         if (e != cudaSuccess) return e;
-        configured[dev] = true;
+        configured[dev].store(true, std::memory_order_release);
     }
     // programmatic dependent launch: the CTAs may start while the grid before this one in
     // the stream (the suffix decode, which triggers at its start) still runs; nothing here
