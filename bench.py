@@ -10,7 +10,7 @@ writes 256 MiB before each step instead).
 
 Prints one JSON line.  value = algorithmic bytes of the step / step time (GB/s);
 tokens/s/layer = sequences / step time.  --impl reference times the CPU oracle
-(fp64, the machine's host cores) on a bounded sample of the same batch instead.
+(fp64, on the host cores) on a bounded sample of the same batch instead.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload llama13b_b16]
 """
