@@ -144,11 +144,12 @@ def test_block_permutation_gives_bit_identical_output(P, engine):
     assert torch.equal(base, moved)
 
 
+@pytest.mark.parametrize("Pz", [256, 64])   # up to 8 partitions a row, and up to 32
 @pytest.mark.parametrize("engine", [1, 2], ids=["cuda_cores", "tensor_cores"], indirect=True)
-def test_partitions_and_merge_match_oracle(P, engine):
+def test_partitions_and_merge_match_oracle(P, engine, Pz):
     w = workloads.build("parts", dtype="f16", num_q_heads=8, num_kv_heads=4, head_dim=64,
                         block_size=16, context_lens=[0, 5, 512, 1025, 2000], seed=9, device=DEV)
-    Pz, mcl = 256, int(w.context_lens.max())
+    mcl = int(w.context_lens.max())
     nparts = -(-mcl // Pz)
     ws = P.workspace_tensor(P.pkv_partition_workspace_bytes(w.num_seqs, w.num_q_heads,
                                                             w.head_dim, mcl, Pz), DEV)
