@@ -65,13 +65,16 @@ WsLayout ws_layout(int32_t S, int32_t Hq, int32_t D, int32_t parts) {
 }
 
 // One pass while the longest context is at most 3072 tokens; beyond that,
-// 1024-token partitions (a multiple of 16 and 32).  Measured on the batches
-// here: one pass was best for the LLaMA-7B (max 2048) and shared-prefix GQA
-// (max 2560) batches, 1024-token partitions for LLaMA-13B (max 4096, a long
-// lognormal tail) and the 32k-128k contexts.
-int32_t auto_partition(const pkv_pool* pool, int32_t max_context_len) {
+// 1024-token partitions (a multiple of 16 and 32), or 2048 with several query rows
+// per sequence, whose partial results and merge cost num_queries times as much.
+// Measured on the batches here: one pass was best for the LLaMA-7B (max 2048) and
+// shared-prefix GQA (max 2560) batches, 1024-token partitions for LLaMA-13B (max
+// 4096, a long lognormal tail) and the 32k-128k contexts; on the LLaMA-13B batch
+// with 4 / 8 new tokens per sequence 2048-token partitions took 346.0 / 362.9 us
+// against 348.6 / 371.8 us with 1024.
+int32_t auto_partition(const pkv_pool* pool, int32_t max_context_len, int32_t num_queries = 1) {
     const int32_t B = pool->block_size;
-    const int32_t one_pass_limit = 3072, split = 1024;
+    const int32_t one_pass_limit = 3072, split = num_queries > 1 ? 2048 : 1024;
     if (max_context_len <= one_pass_limit)
         return max_context_len <= 0 ? B : ceil_div(max_context_len, B) * B;
     return split;
@@ -126,7 +129,7 @@ pkv_status run_decode(const DecodeArgs& a, void* out, int32_t out_dtype, int dir
                       void* workspace, size_t workspace_bytes, cudaStream_t stream,
                       const AppendArgs* append = nullptr) {
     const pkv_pool* pool = a.pool;
-    const int32_t P = a.P > 0 ? a.P : auto_partition(pool, a.max_ctx);
+    const int32_t P = a.P > 0 ? a.P : auto_partition(pool, a.max_ctx, a.NQ);
     const int32_t parts = a.max_ctx > 0 ? ceil_div(a.max_ctx, P) : 1;
     if (parts > 65535) return PKV_ERR_UNSUPPORTED;
     const bool need_ws = !direct || parts > 1;
