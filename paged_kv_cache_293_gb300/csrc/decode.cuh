@@ -243,6 +243,9 @@ paged_decode_kernel(const DecodeParams p) {
             }
             if (p.slot_out && kvh == 0 && lane == 0)
                 p.slot_out[s] = ok ? (int64_t)phys_new * B + (p_new % B) : -1;
+            // the spliced rows are ordinary stores: order them before any later bulk copy
+            // into this stage (none today: the new token's chunk is the warp's last)
+            fence_proxy_async_shared();
             __syncwarp();
         }
         if (!((bad_stages >> st) & 1)) {

@@ -271,6 +271,9 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int tok_end = min(ctx, tok0 + P);
     const int n_chunks = (tok_end - tok0 + CHUNK_TOKENS - 1) / CHUNK_TOKENS;
     const int n_my = warp < n_chunks ? (n_chunks - warp + NW - 1) / NW : 0;
+    // the chunk of this warp's i-th step (chunks are dealt round-robin), and the owner of c
+    auto chunk_of = [&](int i) -> int { return warp + NW * i; };
+    auto owner = [&](int c) -> int { return c % NW; };
 
     // ---- Q^T as mma B fragments: column n = g4 (zero past the live columns), rows = dims
     uint32_t qb[KS][2];
@@ -308,7 +311,7 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
         p.k_new != nullptr && NQn == 1 && !ctx_bad && p_new >= tok0 && p_new < tok_end;
     const bool multi_new = MULTI_APPEND && p.k_new != nullptr && NQn > 1 && !ctx_bad;
     const int c_new = has_new ? (p_new - tok0) / CHUNK_TOKENS : -1;
-    const bool warp_new = has_new && (c_new % NW) == warp;
+    const bool warp_new = has_new && owner(c_new) == warp;
     constexpr int VPR = D * 2 / 16;  // 16-byte vectors per row
     uint4 k_row = make_uint4(0, 0, 0, 0), v_row = make_uint4(0, 0, 0, 0);
     int phys_new = -1;
@@ -323,7 +326,7 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
     auto table_entry = [&](int i) -> int {
         if (i >= n_my) return -1;
-        const int t = tok0 + (warp + NW * i) * CHUNK_TOKENS;
+        const int t = tok0 + chunk_of(i) * CHUNK_TOKENS;
         return __ldg(bt_row + t / B);
     };
     int ids = table_entry(lane);
@@ -338,7 +341,7 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
         if (lane == 0) {
             const uint32_t bar = bar0 + st * 8;
             if (ok) {
-                const int t = tok0 + (warp + NW * i) * CHUNK_TOKENS;
+                const int t = tok0 + chunk_of(i) * CHUNK_TOKENS;
                 const int row = (phys * Hkv + kvh) * B + (t % B);
                 const uint32_t dst = ring_s + st * Geo::STAGE_BYTES;
                 mbar_arrive_expect_tx(bar, Geo::STAGE_BYTES);
@@ -375,7 +378,9 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
         // warp barrier put them ahead of the copies lane 0 issues from here on
         if (multi_new && ctx - NQn < tok_end) {
             const int c_lo = max(ctx - NQn - tok0, 0) / CHUNK_TOKENS;
-            for (int c = c_lo + ((warp - c_lo) % NW + NW) % NW; c < n_chunks; c += NW) {
+            for (int i = 0; i < n_my; ++i) {
+                const int c = chunk_of(i);
+                if (c < c_lo) continue;
                 const int t_c = tok0 + c * CHUNK_TOKENS;
                 append_rows_to_pool<T, D>(p, bt_row, s, kvh, ctx, max(ctx - NQn, t_c),
                                           min(tok_end, t_c + CHUNK_TOKENS), lane);
@@ -398,11 +403,15 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
             for (int j = i + 1; j < n_my && j < i + NS; ++j) mbar_wait(bar0 + (j % NS) * 8, (j / NS) & 1);
             break;
         }
-        const int c = warp + NW * i;
+        const int c = chunk_of(i);
         const int valid = min(CHUNK_TOKENS, tok_end - (tok0 + c * CHUNK_TOKENS));
         unsigned char* Ks = ring + st * Geo::STAGE_BYTES;
         unsigned char* Vs = Ks + Geo::POOL_BYTES;
+        // ordinary stores into this stage below (spliced rows, zeroed rows) must be ordered
+        // before the tensor copy that refills it
+        bool dirty = false;
         if (warp_new && c == c_new) {
+            dirty = true;
             const bool ok = (unsigned)phys_new < (unsigned)p.num_blocks;
             if (ok && lane < VPR) {
                 const int r = (p_new - tok0) & (CHUNK_TOKENS - 1);
@@ -419,11 +428,14 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
         }
         if constexpr (MULTI_APPEND) {
             const int t_c = tok0 + c * CHUNK_TOKENS;
-            if (multi_new && i < NS && t_c + CHUNK_TOKENS > ctx - NQn)
+            if (multi_new && i < NS && t_c + CHUNK_TOKENS > ctx - NQn) {
                 append_rows_into_chunk<T, D>(p, Ks, Vs, s, kvh, ctx, t_c, lane);
+                dirty = true;
+            }
         }
         if (!((bad_stages >> st) & 1)) {
             if (valid < CHUNK_TOKENS) {
+                dirty = true;
                 // rows past the context may hold anything: zero them so 0 * row stays 0
                 for (int v = lane; v < (CHUNK_TOKENS - valid) * VPR; v += 32) {
                     const int r = valid + v / VPR, col = v % VPR;
@@ -496,6 +508,7 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 Mma<T>::run(o[mt], a0, a1, a2, a3, bl0, bl1);
             }
         }
+        if (dirty) fence_proxy_async_shared();
         __syncwarp();
         if (i + NS < n_my) issue(i + NS);
     }

@@ -131,15 +131,17 @@ __device__ __forceinline__ unsigned long long global_ns() {
     return t;
 }
 
-// Wait for phase `parity` of the barrier; false after WAIT_LIMIT_NS.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Wait for phase `parity` of the barrier; false once limit_ns nanoseconds have passed
+// without it completing (the caller then sets PKV_DEVERR_TIMEOUT and stops).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          unsigned long long limit_ns = WAIT_LIMIT_NS) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (global_ns() - t0 > WAIT_LIMIT_NS) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     }
 }
 
@@ -171,6 +173,12 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 // proxy) reads of the same addresses.
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Order this thread's generic-proxy writes to shared memory (st.shared, cp.async) before a
+// later bulk or tensor copy (async proxy) that overwrites the same bytes.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // Wait for this thread's cp.async copies.

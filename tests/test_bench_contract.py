@@ -50,3 +50,39 @@ def test_reference_arm_on_other_ranks_does_no_work():
 def test_bad_arguments_are_refused(args):
     proc = _run("--impl", "reference", *args, timeout=120)
     assert proc.returncode != 0
+
+
+def test_both_arms_print_the_same_config():
+    """The oracle arm's `config` is the GPU arm's: the same function builds both."""
+    import argparse
+    sys.path.insert(0, ROOT)
+    import bench
+    from paged_kv_cache_293_gb300 import workloads
+    proc = _run("--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "3")
+    assert proc.returncode == 0, proc.stderr[-2000:]
+    ref = json.loads(proc.stdout.strip().splitlines()[-1])["config"]
+    args = argparse.Namespace(workload="tiny", seed=0, l2="alternate")
+    ours = bench.workload_config(workloads.make("tiny", seed=0), args, 1)
+    assert ref == json.loads(json.dumps(ours))
+
+
+def test_clock_summary_uses_the_timed_region_then_the_whole_phase():
+    sys.path.insert(0, ROOT)
+    import bench
+    c = bench.ClockSampler.__new__(bench.ClockSampler)
+    row = lambda sm, util, cap: [str(sm), "2070", str(util), "0x0", "Not Active", "Not Active",
+                                 "Not Active", "Active" if cap else "Not Active"]
+    c.lines = [(1.0, row(600, 0, False)), (2.0, row(2070, 99, False)),
+               (3.0, row(2040, 98, True)), (9.0, row(1980, 97, False))]
+    c.fast, c.nvml = [], None
+    c.windows = [(2.5, 3.5)]                       # one nvidia-smi sample inside
+    s = c.summary()
+    assert s["sm_mhz"] == 2040 and s["samples"] == 1 and s["sm_max_mhz"] == 2070
+    assert s["phase"]["sm_mhz"] == 2040 and s["phase"]["samples"] == 3   # idle sample left out
+    assert s["reasons"] == ["sw_power_cap"]
+    c.windows = [(4.0, 4.01)]                      # a timed region too short for a sample
+    s = c.summary()
+    assert s["samples"] == 0 and s["sm_mhz"] == s["phase"]["sm_mhz"]
+    c.fast = [(4.005, 2055.0, []), (4.008, 2065.0, [])]   # NVML samples inside it
+    s = c.summary()
+    assert s["samples"] == 2 and s["sm_mhz"] == 2060.0 and "NVML" in s["source"]
