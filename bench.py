@@ -80,23 +80,80 @@ def read_traffic(workload):
         return None
 
 
+class _Nvml:
+    """Read-only NVML queries through ctypes: the SM clock and the clock-event (throttle)
+    reasons, fast enough to poll every millisecond during a short timed region."""
+    SM = 1   # NVML_CLOCK_SM
+    REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                   0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, uuid, index):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        rc = self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) if uuid else 1
+        if rc != 0:
+            rc = self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h))
+        if rc != 0:
+            raise OSError("no NVML handle")
+        try:
+            self._reasons = self.lib.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            self._reasons = self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        self.max_mhz = (mx.value if self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.SM,
+                                                                       ctypes.byref(mx)) == 0
+                        else None)
+
+    def sample(self):
+        c, r = self.ct.c_uint(), self.ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, self.SM, self.ct.byref(c)) != 0:
+            return None
+        self._reasons(self.h, self.ct.byref(r))
+        return float(c.value), [n for bit, n in self.REASON_BITS.items() if r.value & bit]
+
+
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons while the timed region runs."""
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """SM clocks and throttle reasons of this GPU, read (never set) two ways:
+
+    - `nvidia-smi -lms 50` runs from start() to stop() (warm-up, timed region and the
+      end-to-end leg: the whole GPU phase), each sample stamped by nvidia-smi itself;
+    - inside timed() an NVML poll every millisecond, so that even a timed region of a few
+      milliseconds has samples of its own.
+
+    summary() gives the timed region's median clock and the reasons seen in it (NVML
+    samples, else the nvidia-smi samples stamped inside it), and the whole phase's median
+    over the samples taken under load."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,utilization.gpu,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, index):
-        self.index = index
+    def __init__(self, device):
+        self.index = device.index or 0
+        try:
+            u = str(torch.cuda.get_device_properties(device).uuid)
+            self.uuid = u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            self.uuid = None
         self.proc = None
-        self.lines = []
+        self.lines = []          # (wall time from nvidia-smi's stamp, fields)
+        self.fast = []           # (wall time, sm MHz, reasons) from NVML inside timed()
+        self.windows = []
+        try:
+            self.nvml = _Nvml(self.uuid, self.index)
+        except Exception:
+            self.nvml = None
 
-    def __enter__(self):
+    def start(self):
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                ["nvidia-smi", "-i", self.uuid or str(self.index), "--query-gpu=" + self.FIELDS,
                  "--format=csv,noheader,nounits", "-lms", "50"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except (OSError, ValueError):
@@ -104,10 +161,48 @@ class ClockSampler:
         return self
 
     def _read(self):
+        import datetime
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            parts = [p.strip() for p in line.split(",")]
+            try:
+                t = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except (ValueError, IndexError):
+                t = time.time()
+            self.lines.append((t, parts[1:]))
 
-    def __exit__(self, *exc):
+    def wait_first(self, timeout=5.0):
+        """Block until nvidia-smi has delivered a sample (or the timeout passes)."""
+        t = time.time()
+        while self.proc is not None and not self.lines and time.time() - t < timeout:
+            time.sleep(0.02)
+
+    def timed(self):
+        sampler = self
+
+        class _Window:
+            def __enter__(self):
+                self.stop = threading.Event()
+                self.t0 = time.time()
+                if sampler.nvml is not None:
+                    self.th = threading.Thread(target=self._poll, daemon=True)
+                    self.th.start()
+                return self
+
+            def _poll(self):
+                while not self.stop.is_set():
+                    r = sampler.nvml.sample()
+                    if r is not None:
+                        sampler.fast.append((time.time(), r[0], r[1]))
+                    self.stop.wait(0.001)
+
+            def __exit__(self, *exc):
+                self.stop.set()
+                if sampler.nvml is not None:
+                    self.th.join(timeout=2)
+                sampler.windows.append((self.t0, time.time()))
+        return _Window()
+
+    def stop(self):
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -116,27 +211,58 @@ class ClockSampler:
                 self.proc.kill()
             self.thread.join(timeout=2)
 
-    def summary(self):
-        if self.proc is None or not self.lines:
-            return None
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
-            parts = [p.strip() for p in line.split(",")]
+    def __enter__(self):
+        self.start()
+        self._win = self.timed()
+        self._win.__enter__()
+        return self
+
+    def __exit__(self, *exc):
+        self._win.__exit__(*exc)
+        self.stop()
+
+    def _smi(self):
+        out = []
+        for t, parts in self.lines:
             if len(parts) < 8:
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
+                sm, mx = float(parts[0]), float(parts[1])
             except ValueError:
                 continue
-            for n, v in zip(names, parts[4:8]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
+            try:
+                util = float(parts[2])
+            except ValueError:
+                util = 100.0
+            rs = [n for n, v in zip(self.NAMES, parts[4:8]) if v.lower().startswith("active")]
+            out.append((t, sm, mx, util, rs))
+        return out
+
+    def summary(self):
+        smi = self._smi()
+        if not smi and not self.fast:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        inside = lambda t: any(a <= t <= b for a, b in self.windows)
+        if self.fast:
+            timed = [(sm, rs) for t, sm, rs in self.fast]
+            source = "NVML every 1 ms inside the timed region"
+        else:
+            timed = [(sm, rs) for t, sm, mx, u, rs in smi if inside(t)]
+            source = "nvidia-smi every 50 ms inside the timed region"
+        load = [(sm, rs) for t, sm, mx, u, rs in smi if u >= 50.0] or \
+               [(sm, rs) for t, sm, mx, u, rs in smi]
+        mx = [m for _, _, m, _, _ in smi] + ([self.nvml.max_mhz] if self.nvml and
+                                              self.nvml.max_mhz else [])
+        phase = {"sm_mhz": statistics.median(x for x, _ in load) if load else None,
+                 "reasons": sorted({r for _, rs in load for r in rs}), "samples": len(load),
+                 "source": "nvidia-smi every 50 ms, warm-up to end of the e2e leg, samples with "
+                           "GPU utilisation >= 50 %"}
+        med = statistics.median(x for x, _ in timed) if timed else phase["sm_mhz"]
+        return {"sm_mhz": med, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted({r for _, rs in timed for r in rs} | set(phase["reasons"])),
+                "samples": len(timed),
+                "source": source if timed else "no sample inside the timed region: whole phase",
+                "phase": phase}
 
 
 def dist_setup(gpus):
@@ -168,7 +294,7 @@ def max_over_ranks(x, world, device):
 class Step:
     """Device buffers and the launch sequence of one decode step through the binding."""
 
-    def __init__(self, P, w, device, fused=True, cascade=True):
+    def __init__(self, P, w, device, fused=True, cascade=False):
         self.P, self.w, self.dev, self.fused = P, w, device, fused
         # batches whose sequences share prefix blocks: the prefix's attention once per kv
         # head on tensor cores, then each sequence's own suffix, then the merge
@@ -246,6 +372,32 @@ def step_bytes(w, psize):
     return dec_logical, dec_unique, other
 
 
+def l2_mode_for(w, args):
+    """How the GPU arm keeps its timed steps L2-cold on this batch: two pools alternate, or
+    (a pool smaller than twice the L2 would not be evicted by alternating) a flush."""
+    return args.l2 if 2 * (w.k_pool.nbytes + w.v_pool.nbytes) > FLUSH_BYTES else "flush"
+
+
+def workload_config(w, args, world):
+    """The `config` of the JSON line: the batch both arms run (the GPU arm and the oracle
+    arm print the same dict for the same flags)."""
+    return {
+        "workload": w.name, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
+        "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+        "context_lens": LENGTH_RECIPES.get(args.workload, ""),
+        "mean_context": round(float(w.context_lens.mean()), 1),
+        "max_context": w.max_context_len, "pool_blocks": w.num_blocks,
+        "kv_bytes_per_step": int(w.context_lens.sum()) * accounting.kv_bytes_per_token(
+            w.num_kv_heads, w.head_dim, workloads.ELEM_BYTES[w.dtype]),
+        "l2": ("GPU arm: consecutive steps alternate between two KV pools of this shape (two "
+               "layers' caches, each larger than L2)" if l2_mode_for(w, args) == "alternate" else
+               "GPU arm: flushed by a 256 MiB write before every timed step (outside the "
+               "events)"),
+        "parallelism": "replicas, one batch per GPU" if world > 1 else "single GPU",
+        "seed": args.seed,
+    }
+
+
 def cpu_oracle_rate(w, budget_s=12.0, max_single_s=30.0):
     """Time the oracle (as it stands) on host copies of a bounded sample of the batch."""
     import oracle
@@ -294,7 +446,7 @@ def run_ours(args):
     # 256 MiB before each step (outside the events), which leaves dirty lines in L2 that the
     # timed step then has to write back.
     # (a pool smaller than twice the L2 is flushed instead: alternating would not evict it)
-    l2_mode = args.l2 if 2 * (w.k_pool.nbytes + w.v_pool.nbytes) > FLUSH_BYTES else "flush"
+    l2_mode = l2_mode_for(w, args)
     pools = [(w.k_pool, w.v_pool), (w.k_pool.clone(), w.v_pool.clone())]
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device) if l2_mode == "flush" else None
     stream = torch.cuda.current_stream(device)
@@ -306,6 +458,8 @@ def run_ours(args):
         else:
             w.k_pool, w.v_pool = pools[i % 2]
 
+    clocks = ClockSampler(device).start()
+    clocks.wait_first()
     for i in range(args.warmup):
         prepare(i)
         st.pre_decode()
@@ -317,7 +471,7 @@ def run_ours(args):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize(device)
-    with ClockSampler(device.index) as clocks:
+    with clocks.timed():
         t_wall = time.perf_counter()
         for i in range(args.steps):
             prepare(i)
@@ -339,6 +493,7 @@ def run_ours(args):
     # end to end through the binding with host buffers: H2D inputs, the step, D2H output
     e2e = run_e2e(P, w, st, args, device, pools)
     w.k_pool, w.v_pool = pools[0]
+    clocks.stop()
     e2e_ms_max = max_over_ranks(e2e["ms"], world, device)
 
     dec_logical, dec_unique, other = step_bytes(w, st.psize if st.split and not st.prefix_len else 0)
@@ -390,25 +545,12 @@ def run_ours(args):
         "tokens_per_s_per_layer": round(world * w.num_seqs / (step_ms_max * 1e-3), 1),
         "pct_of_peak": round(100.0 * value / world / peak, 2),
         "decode_ms": round(dec_ms, 5),
-        "config": {
-            "workload": w.name, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
-            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
-            "context_lens": LENGTH_RECIPES.get(args.workload, ""),
-            "mean_context": round(float(w.context_lens.mean()), 1),
-            "max_context": w.max_context_len, "partition_size": st.psize if st.split else 0,
-            "pool_blocks": w.num_blocks,
-            "kv_bytes_per_step": int(w.context_lens.sum()) * accounting.kv_bytes_per_token(
-                w.num_kv_heads, w.head_dim, workloads.ELEM_BYTES[w.dtype]),
-            "l2": ("consecutive steps alternate between two KV pools of this shape (two layers' "
-                   "caches, each larger than L2)" if l2_mode == "alternate" else
-                   "flushed by a 256 MiB write before every timed step (outside the events)"),
-            "parallelism": "replicas, one batch per GPU" if world > 1 else "single GPU",
-            "seed": args.seed,
-            "path": ("decode with the append fused (slot, write, attention in one launch)"
-                     if st.fused else "slot mapping, cache write, decode: three launches")
-                    + ("; cascade over the %d-token shared prefix" % st.prefix_len
-                       if st.prefix_len else ""),
-        },
+        "config": workload_config(w, args, world),
+        "partition_size": st.psize if st.split else 0,
+        "path": ("decode with the append fused (slot, write, attention in one launch)"
+                 if st.fused else "slot mapping, cache write, decode: three launches")
+                + ("; cascade over the %d-token shared prefix" % st.prefix_len
+                   if st.prefix_len else ""),
         "roofline": {
             "kernel": kernel_name,
             "bound": "hbm", "achieved": round(dec_gbs, 2), "peak": peak, "unit": "GB/s",
@@ -567,10 +709,7 @@ def run_reference(args):
         "ms_per_step": round(sec * 1e3, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "tokens_per_s_per_layer": round(n / sec, 2),
-        "config": {"workload": w.name, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
-                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
-                   "block_size": w.block_size,
-                   "context_lens": LENGTH_RECIPES.get(args.workload, ""), "seed": args.seed},
+        "config": workload_config(w, args, world),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "kind": "oracle",
                          "cores": oracle.num_threads(), "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -590,7 +729,7 @@ def _time_steps(device, stream, steps, warmup, prepare, body):
     torch.cuda.synchronize(device)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)]
-    with ClockSampler(device.index) as clocks:
+    with ClockSampler(device) as clocks:
         for i in range(steps):
             prepare(i)
             evs[i][0].record(stream)
