@@ -14,11 +14,11 @@
 // probabilities enter the P.V product with about 16 significant bits instead of
 // the 8 of a single bf16 rounding.
 //
-// Pages are staged by TMA tensor copies (cp.async.bulk.tensor.2d) through a
-// tensor map over the pool viewed as [rows = N*Hkv*B][D]: a 16-token chunk of a
-// page is D*2/128 boxes of [16 rows][64 elements] per pool, landing in shared
-// memory with the 128-byte swizzle, which makes the ldmatrix reads of both K
-// (row-major) and V (transposed) free of bank conflicts.  Each warp runs its
+// Pages are staged by TMA tensor copies (cp.async.bulk.tensor.3d) through a
+// tensor map over the pool viewed as [rows = N*Hkv*B][D / 64][64]: one copy per
+// pool brings a 16-token chunk of a page as D*2/128 boxes of [16 rows][64
+// elements], landing in shared memory with the 128-byte swizzle, which makes the
+// ldmatrix reads of both K (row-major) and V (transposed) free of bank conflicts.  Each warp runs its
 // own mbarrier ring exactly as in decode.cuh; the NW warp states are combined
 // in shared memory at the end.
 #pragma once
@@ -40,6 +40,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// One copy of a 3-D box: the D/64 column halves of a chunk's rows land as consecutive
+// [16 rows][128 bytes] swizzled boxes, the same layout as D/64 2-D copies.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
         : "memory");
 }
 
@@ -200,6 +211,90 @@ __device__ __forceinline__ void append_rows_into_chunk(const DecodeParams& p, un
     __syncwarp();
 }
 
+// One staged 16-token chunk (K rows at ks_s, V rows at vs_s, 128-byte swizzled boxes)
+// into the running state of the 8 columns of the N tile held by this lane (columns
+// 2 q4 and 2 q4 + 1; the o fragments cover tokens g4 and g4 + 8 of each m16 tile):
+//   scores^T = K . Q^T on D/16 MMAs; token t of the chunk counts for column h when
+//   t < valid and chunk0 + t < lim[h] (else its score is -inf); online softmax per
+//   column in base 2; O^T += V^T . P^T with P as a 16-bit high part plus remainder.
+// V rows >= valid must hold zeros.  A column whose tokens are all masked is left exactly
+// as it was (alpha = 1, p = 0).
+template <typename T, int D>
+__device__ __forceinline__ void mma_chunk_update(uint32_t ks_s, uint32_t vs_s,
+                                                 const uint32_t (&qb)[D / 16][2], int chunk0,
+                                                 int valid, const int (&lim)[2], float scale_log2,
+                                                 float (&m)[2], float (&l)[2],
+                                                 float (&o)[D / 16][4], int lane) {
+    using Geo = MmaGeometry<D>;
+    constexpr int KS = Geo::KSTEPS;
+    const int g4 = lane >> 2, q4 = lane & 3;
+    // ldmatrix row addresses: matrix mi = lane / 8, row lane % 8
+    const int mi = lane >> 3, mr = lane & 7;
+    // P^T fragment sources: tokens 2 q4 + e come from lane 8 q4 + 4 e + lane / 8
+    const int src0 = 8 * q4 + (lane >> 3), src1 = src0 + 4;
+    const uint32_t sel = ((lane >> 2) & 1) ? 0x7632u : 0x5410u;
+    // scores^T = K . Q^T
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+        const int col = 2 * ks + (mi >> 1);            // 16-byte column of dims
+        const int r = ((mi & 1) << 3) + mr;
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(ks_s + (col / 8) * Geo::BOX_BYTES + swz(r, col & 7), a0, a1, a2, a3);
+        Mma<T>::run(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+    }
+    // online softmax per head column (tokens g4 and g4 + 8 of this lane)
+    float pr[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int tok = g4 + ((j >> 1) << 3);
+        pr[j] = (tok < valid && chunk0 + tok < lim[j & 1]) ? sc[j] * scale_log2 : -INFINITY;
+    }
+    float alpha[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        float bm = fmaxf(pr[h], pr[h + 2]);
+#pragma unroll
+        for (int o_ = 4; o_ < 32; o_ <<= 1) bm = fmaxf(bm, __shfl_xor_sync(FULL_MASK, bm, o_));
+        const float mn = fmaxf(m[h], bm);
+        const float mref = mn == -INFINITY ? 0.f : mn;   // column fully masked so far
+        alpha[h] = fast_exp2(m[h] - mref);
+        m[h] = mn;
+        pr[h] = fast_exp2(pr[h] - mref);
+        pr[h + 2] = fast_exp2(pr[h + 2] - mref);
+        l[h] = l[h] * alpha[h] + pr[h] + pr[h + 2];
+    }
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+        o[mt][0] *= alpha[0]; o[mt][1] *= alpha[1];
+        o[mt][2] *= alpha[0]; o[mt][3] *= alpha[1];
+    }
+    // P^T as B fragments, high part and remainder
+    float rem[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) rem[j] = pr[j] - Mma<T>::round_trip(pr[j]);
+    const uint32_t lo_hi = Mma<T>::pack(pr[0], pr[1]), hi_hi = Mma<T>::pack(pr[2], pr[3]);
+    const uint32_t lo_lo = Mma<T>::pack(rem[0], rem[1]), hi_lo = Mma<T>::pack(rem[2], rem[3]);
+    const uint32_t bh0 = __byte_perm(__shfl_sync(FULL_MASK, lo_hi, src0),
+                                     __shfl_sync(FULL_MASK, lo_hi, src1), sel);
+    const uint32_t bh1 = __byte_perm(__shfl_sync(FULL_MASK, hi_hi, src0),
+                                     __shfl_sync(FULL_MASK, hi_hi, src1), sel);
+    const uint32_t bl0 = __byte_perm(__shfl_sync(FULL_MASK, lo_lo, src0),
+                                     __shfl_sync(FULL_MASK, lo_lo, src1), sel);
+    const uint32_t bl1 = __byte_perm(__shfl_sync(FULL_MASK, hi_lo, src0),
+                                     __shfl_sync(FULL_MASK, hi_lo, src1), sel);
+    // O^T += V^T . P^T
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+        const int col = 2 * mt + (mi & 1);
+        const int r = ((mi >> 1) << 3) + mr;
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_trans(vs_s + (col / 8) * Geo::BOX_BYTES + swz(r, col & 7), a0, a1, a2, a3);
+        Mma<T>::run(o[mt], a0, a1, a2, a3, bh0, bh1);
+        Mma<T>::run(o[mt], a0, a1, a2, a3, bl0, bl1);
+    }
+}
+
 template <typename T, int D, int NW, int NS, bool MULTI_APPEND = false>
 __global__ void __launch_bounds__(NW * 32)
 paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
@@ -345,12 +440,9 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 const int row = (phys * Hkv + kvh) * B + (t % B);
                 const uint32_t dst = ring_s + st * Geo::STAGE_BYTES;
                 mbar_arrive_expect_tx(bar, Geo::STAGE_BYTES);
-#pragma unroll
-                for (int b = 0; b < Geo::BOXES; ++b) {
-                    tma_load_2d(dst + b * Geo::BOX_BYTES, &tmap_k, b * 64, row, bar, policy);
-                    tma_load_2d(dst + Geo::POOL_BYTES + b * Geo::BOX_BYTES, &tmap_v, b * 64, row,
-                                bar, policy);
-                }
+                // one copy per pool: every 128-byte column box of the chunk's 16 rows
+                tma_load_3d(dst, &tmap_k, 0, row, 0, bar, policy);
+                tma_load_3d(dst + Geo::POOL_BYTES, &tmap_v, 0, row, 0, bar, policy);
             } else {
                 set_error(p.err, PKV_DEVERR_BLOCK_ID);
                 mbar_arrive(bar);
@@ -389,12 +481,6 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
             __syncwarp();
         }
     }
-
-    // ldmatrix row addresses: matrix mi = lane / 8, row lane % 8
-    const int mi = lane >> 3, mr = lane & 7;
-    // P^T fragment sources: tokens 2 q4 + e come from lane 8 q4 + 4 e + lane / 8
-    const int src0 = 8 * q4 + (lane >> 3), src1 = src0 + 4;
-    const uint32_t sel = ((lane >> 2) & 1) ? 0x7632u : 0x5410u;
 
     for (int i = 0; i < n_my; ++i) {
         const int st = i % NS;
@@ -444,69 +530,8 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 }
                 __syncwarp();
             }
-            const uint32_t ks_s = smem_addr(Ks), vs_s = smem_addr(Vs);
-
-            // scores^T = K . Q^T
-            float sc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                const int col = 2 * ks + (mi >> 1);            // 16-byte column of dims
-                const int r = ((mi & 1) << 3) + mr;
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4(ks_s + (col / 8) * Geo::BOX_BYTES + swz(r, col & 7), a0, a1, a2, a3);
-                Mma<T>::run(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-            }
-            // online softmax per head column (tokens g4 and g4 + 8 of this lane)
-            float pr[4];
-            const int chunk0 = tok0 + c * CHUNK_TOKENS;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int tok = g4 + ((j >> 1) << 3);
-                pr[j] = (tok < valid && chunk0 + tok < lim[j & 1]) ? sc[j] * p.scale_log2 : -INFINITY;
-            }
-            float alpha[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                float bm = fmaxf(pr[h], pr[h + 2]);
-#pragma unroll
-                for (int o_ = 4; o_ < 32; o_ <<= 1) bm = fmaxf(bm, __shfl_xor_sync(FULL_MASK, bm, o_));
-                const float mn = fmaxf(m[h], bm);
-                const float mref = mn == -INFINITY ? 0.f : mn;   // column fully masked so far
-                alpha[h] = fast_exp2(m[h] - mref);
-                m[h] = mn;
-                pr[h] = fast_exp2(pr[h] - mref);
-                pr[h + 2] = fast_exp2(pr[h + 2] - mref);
-                l[h] = l[h] * alpha[h] + pr[h] + pr[h + 2];
-            }
-#pragma unroll
-            for (int mt = 0; mt < KS; ++mt) {
-                o[mt][0] *= alpha[0]; o[mt][1] *= alpha[1];
-                o[mt][2] *= alpha[0]; o[mt][3] *= alpha[1];
-            }
-            // P^T as B fragments, high part and remainder
-            float rem[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) rem[j] = pr[j] - Mma<T>::round_trip(pr[j]);
-            const uint32_t lo_hi = Mma<T>::pack(pr[0], pr[1]), hi_hi = Mma<T>::pack(pr[2], pr[3]);
-            const uint32_t lo_lo = Mma<T>::pack(rem[0], rem[1]), hi_lo = Mma<T>::pack(rem[2], rem[3]);
-            const uint32_t bh0 = __byte_perm(__shfl_sync(FULL_MASK, lo_hi, src0),
-                                             __shfl_sync(FULL_MASK, lo_hi, src1), sel);
-            const uint32_t bh1 = __byte_perm(__shfl_sync(FULL_MASK, hi_hi, src0),
-                                             __shfl_sync(FULL_MASK, hi_hi, src1), sel);
-            const uint32_t bl0 = __byte_perm(__shfl_sync(FULL_MASK, lo_lo, src0),
-                                             __shfl_sync(FULL_MASK, lo_lo, src1), sel);
-            const uint32_t bl1 = __byte_perm(__shfl_sync(FULL_MASK, hi_lo, src0),
-                                             __shfl_sync(FULL_MASK, hi_lo, src1), sel);
-            // O^T += V^T . P^T
-#pragma unroll
-            for (int mt = 0; mt < KS; ++mt) {
-                const int col = 2 * mt + (mi & 1);
-                const int r = ((mi >> 1) << 3) + mr;
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4_trans(vs_s + (col / 8) * Geo::BOX_BYTES + swz(r, col & 7), a0, a1, a2, a3);
-                Mma<T>::run(o[mt], a0, a1, a2, a3, bh0, bh1);
-                Mma<T>::run(o[mt], a0, a1, a2, a3, bl0, bl1);
-            }
+            mma_chunk_update<T, D>(smem_addr(Ks), smem_addr(Vs), qb, tok0 + c * CHUNK_TOKENS, valid,
+                                   lim, p.scale_log2, m, l, o, lane);
         }
         if (dirty) fence_proxy_async_shared();
         __syncwarp();
@@ -597,6 +622,25 @@ inline bool encode_pool_map(CUtensorMap* map, const void* base, long long rows, 
            CUDA_SUCCESS;
 }
 
+// The pool seen as a 3-D tensor for the decode kernel: x = 64 elements of a 128-byte
+// column box, y = rows (N * Hkv * B), z = which 128-byte column of the row (D / 64 of
+// them); strides D * 2 bytes (y) and 128 bytes (z).  A box of {64, 16, D / 64} is a whole
+// 16-token chunk of one pool, landing as D / 64 consecutive [16][128-byte] boxes with the
+// 128-byte swizzle: one copy per pool and chunk instead of D / 64.
+template <typename T>
+inline bool encode_pool_map_3d(CUtensorMap* map, const void* base, long long rows, int D) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(D / 64)};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * sizeof(T), 128};
+    const cuuint32_t box[3] = {64, (cuuint32_t)CHUNK_TOKENS, (cuuint32_t)(D / 64)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, Mma<T>::TMA_TYPE, 3, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 template <int D> struct MmaShape { static constexpr int NW = 4, NS = (64 * 1024) / (4 * MmaGeometry<D>::STAGE_BYTES); };
 
 template <typename T, int D, bool MULTI_APPEND>
@@ -607,12 +651,13 @@ cudaError_t launch_decode_mma_tdv(const DecodeParams& p, cudaStream_t stream) {
     CUtensorMap tk, tv;
     const long long rows = (long long)p.num_blocks * p.num_kv_heads * p.block_size;
     if (rows >= (1ll << 31)) return cudaErrorNotSupported;  // TMA row coordinates are int32
-    if (!encode_pool_map<T>(&tk, p.k_pool, rows, D) || !encode_pool_map<T>(&tv, p.v_pool, rows, D))
+    if (!encode_pool_map_3d<T>(&tk, p.k_pool, rows, D) ||
+        !encode_pool_map_3d<T>(&tv, p.v_pool, rows, D))
         return cudaErrorNotSupported;
-    auto kernel = paged_decode_mma_kernel<T, D, NW, NS, MULTI_APPEND>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    auto kernel = paged_decode_mma_kernel<T, D, NW, NS, MULTI_APPEND>;
     static std::atomic<bool> configured[64];  // per device; setting it twice is harmless
     if (dev < 64 && !configured[dev].load(std::memory_order_acquire)) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
