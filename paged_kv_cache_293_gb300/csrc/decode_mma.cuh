@@ -18,9 +18,10 @@
 // tensor map over the pool viewed as [rows = N*Hkv*B][D / 64][64]: one copy per
 // pool brings a 16-token chunk of a page as D*2/128 boxes of [16 rows][64
 // elements], landing in shared memory with the 128-byte swizzle, which makes the
-// ldmatrix reads of both K (row-major) and V (transposed) free of bank conflicts.  Each warp runs its
-// own mbarrier ring exactly as in decode.cuh; the NW warp states are combined
-// in shared memory at the end.
+// ldmatrix reads of both K (row-major) and V (transposed) free of bank conflicts.
+// Each warp runs its own mbarrier ring as in decode.cuh, but walks its chunks
+// alternately from the front and the back of its list (alternating_chunk); the
+// NW warp states are combined in shared memory at the end.
 #pragma once
 
 #include <cuda.h>
@@ -366,8 +367,9 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int tok_end = min(ctx, tok0 + P);
     const int n_chunks = (tok_end - tok0 + CHUNK_TOKENS - 1) / CHUNK_TOKENS;
     const int n_my = warp < n_chunks ? (n_chunks - warp + NW - 1) / NW : 0;
-    // the chunk of this warp's i-th step (chunks are dealt round-robin), and the owner of c
-    auto chunk_of = [&](int i) -> int { return warp + NW * i; };
+    // the chunk of this warp's i-th step (chunks are dealt round-robin, each warp walks its
+    // own alternately from the front and the back), and the owner of chunk c
+    auto chunk_of = [&](int i) -> int { return warp + NW * alternating_chunk(i, n_my); };
     auto owner = [&](int c) -> int { return c % NW; };
 
     // ---- Q^T as mma B fragments: column n = g4 (zero past the live columns), rows = dims

@@ -196,6 +196,23 @@ __device__ __forceinline__ void set_error(unsigned int* err, unsigned int bits) 
     atomicOr(err, bits);
 }
 
+// ------------------------------------------------------------------ chunk order
+
+// Order in which a warp of the tensor-core decode kernel walks its n chunks (the warp's
+// k-th chunk in position order is chunk warp + NW * k): alternately one from the front
+// and one from the back of its list -- 0, n-1, 1, n-2, ...  When sequences share their
+// first blocks (a common prefix, "Serving models with vLLM", section "How it works:
+// PagedAttention"), the front chunks are mostly served from L2 and the back ones from
+// DRAM; alternating keeps every warp's DRAM copies in flight while it works through the
+// shared chunks, instead of a run of L2-only steps at the start of each CTA (measured
+// 4-5 us faster on a 256-sequence batch sharing 512 tokens, neutral without sharing; the
+// CUDA-core kernel, which serves MHA batches, measured about 1 % slower with it and keeps
+// the plain order).  The order depends on logical positions only, so results still do
+// not depend on where blocks sit in the pool.
+__device__ __forceinline__ int alternating_chunk(int i, int n) {
+    return (i & 1) ? n - 1 - (i >> 1) : (i >> 1);
+}
+
 // ------------------------------------------------------------------ element types
 
 template <typename T> struct Elem;
