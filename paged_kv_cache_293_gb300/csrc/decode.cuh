@@ -82,7 +82,9 @@ paged_decode_kernel(const DecodeParams p) {
 
     extern __shared__ __align__(128) unsigned char smem[];
 
-    const int kvh = blockIdx.x, s = blockIdx.y, part = blockIdx.z;
+    // partitions launch last-first: the highest ones exist only for the longest sequences,
+    // so the CTAs left running at the end are first partitions, many of them short
+    const int kvh = blockIdx.x, s = blockIdx.y, part = gridDim.z - 1 - blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int B = p.block_size, Hkv = p.num_kv_heads, Hq = p.num_q_heads, P = p.partition_size;
 

@@ -311,7 +311,9 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
     if (p.trigger_dependents) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int Hkv = p.num_kv_heads;
-    const int kvh = blockIdx.x % Hkv, qgrp = blockIdx.x / Hkv, s = blockIdx.y, part = blockIdx.z;
+    // partitions launch last-first, as in decode.cuh
+    const int kvh = blockIdx.x % Hkv, qgrp = blockIdx.x / Hkv, s = blockIdx.y;
+    const int part = gridDim.z - 1 - blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int B = p.block_size, Hq = p.num_q_heads, P = p.partition_size;
     const int G = Hq / Hkv, NQ = p.num_queries;
