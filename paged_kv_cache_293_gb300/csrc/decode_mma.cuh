@@ -611,7 +611,8 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // The pool seen as a 2-D tensor [num_blocks * Hkv * B rows][D], boxes of
-// [16 rows][64 elements] with the 128-byte swizzle.
+// [16 rows][64 elements] with the 128-byte swizzle (the shared-prefix pass in
+// prefix.cuh copies its chunks through this map).
 template <typename T>
 inline bool encode_pool_map(CUtensorMap* map, const void* base, long long rows, int D) {
     auto enc = tensor_map_encoder();
