@@ -108,6 +108,9 @@ class _Nvml:
                                                                        ctypes.byref(mx)) == 0
                         else None)
 
+    def close(self):
+        self.lib.nvmlShutdown()
+
     def sample(self):
         c, r = self.ct.c_uint(), self.ct.c_ulonglong()
         if self.lib.nvmlDeviceGetClockInfo(self.h, self.SM, self.ct.byref(c)) != 0:
@@ -203,6 +206,8 @@ class ClockSampler:
         return _Window()
 
     def stop(self):
+        if self.nvml is not None:
+            self.nvml.close()
         if self.proc is not None:
             self.proc.terminate()
             try:
