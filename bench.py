@@ -400,6 +400,8 @@ def workload_config(w, args, world):
                "events)"),
         "parallelism": "replicas, one batch per GPU" if world > 1 else "single GPU",
         "seed": args.seed,
+        "order": ("the given order" if getattr(args, "order", "given") == "given" else
+                  "the shortest fifth of the sequences last, longest of them first"),
     }
 
 
@@ -445,6 +447,8 @@ def run_ours(args):
     from paged_kv_cache_293_gb300 import pagedkv as P
 
     w = workloads.make(args.workload, seed=args.seed + rank, device=device)
+    if args.order == "shortest-last":   # the batch order a serving engine can choose
+        w = workloads.reorder(w, workloads.shortest_last_order(w.context_lens))
     st = Step(P, w, device, fused=not args.unfused, cascade=args.cascade)
     # Keep every timed step L2-cold: by default consecutive steps read two KV pools of the
     # batch's shape (two layers' caches, each larger than L2); --l2 flush instead writes
@@ -1064,6 +1068,9 @@ def main():
     ap.add_argument("--queries", type=int, default=4, help="new tokens per sequence (--path multi)")
     ap.add_argument("--unfused", action="store_true",
                     help="slot mapping, cache write and decode as three launches")
+    ap.add_argument("--order", choices=["given", "shortest-last"], default="given",
+                    help="sequence order of the batch: as generated (default), or the shortest "
+                         "fifth last, the order a serving engine that knows the lengths can pick")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -273,6 +273,38 @@ def make(name, seed=0, device="cpu", **kw) -> Workload:
     return CONFIGS[name](seed=seed, device=device, **kw)
 
 
+def shortest_last_order(context_lens, fraction=0.2) -> np.ndarray:
+    """A batch order a serving engine can pick on the host, where it knows every
+    sequence's length: the shortest `fraction` of the sequences last (longest of them
+    first), the others in their given order.  GPUs launch a decode grid's CTAs in
+    sequence order, so the CTAs still running when the grid drains are then short ones
+    rather than whatever long sequences happened to come last.  (Fully longest-first is
+    slower: CTAs of equal length finish, and restart, in waves.)"""
+    ctx = np.asarray(context_lens)
+    S = ctx.size
+    k = int(round(fraction * S))
+    by_len = np.argsort(-ctx, kind="stable")           # longest first, ties by index
+    short = by_len[S - k:] if k else np.zeros(0, np.int64)
+    is_short = np.zeros(S, bool)
+    is_short[short] = True
+    return np.concatenate([np.flatnonzero(~is_short), short]).astype(np.int64)
+
+
+def reorder(w: Workload, order) -> Workload:
+    """The same batch with its sequences in `order` (row i = old sequence order[i]); the
+    pools and every sequence's blocks are untouched."""
+    order = np.asarray(order, np.int64)
+    idx = torch.as_tensor(order, device=w.q.device)
+    old_to_new = np.empty_like(order)
+    old_to_new[order] = np.arange(order.size)
+    return dataclasses.replace(
+        w, context_lens=w.context_lens[order].astype(np.int32),
+        block_tables=w.block_tables[order], positions=w.positions[order],
+        q=w.q.index_select(0, idx).contiguous(), k_new=w.k_new.index_select(0, idx).contiguous(),
+        v_new=w.v_new.index_select(0, idx).contiguous(),
+        cow_seqs=old_to_new[w.cow_seqs].astype(np.int32))
+
+
 def storage_numpy(t: torch.Tensor) -> np.ndarray:
     """Host numpy view of a tensor's element storage (fp16 / bf16 as uint16 bits)."""
     t = t.detach().contiguous().cpu()
