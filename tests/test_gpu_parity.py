@@ -620,6 +620,27 @@ def test_bench_step_matches_oracle_at_full_size(P, name, out_dtype):
     assert_no_device_error(P)
 
 
+def test_bench_step_in_shortest_last_order_matches_oracle(P):
+    """bench.py --order shortest-last: the same batch with its shortest fifth last; every
+    sequence's slot, write and attention still match the oracle."""
+    import bench
+    w = workloads.make("gqa_prefix", seed=0, device=DEV)
+    w = workloads.reorder(w, workloads.shortest_last_order(w.context_lens))
+    st = bench.Step(P, w, torch.device(DEV), fused=True, cascade=False)
+    st.out = torch.full_like(st.out, float("nan"), dtype=torch.float32)
+    ref = OracleStep(w, extra_blocks=w.cow_pairs[:, 1], keep_device_clone=True)
+    ref.copy_blocks(w.cow_pairs)
+    ref.write()
+    st.pre_decode()
+    st.decode()
+    torch.cuda.synchronize()
+    assert np.array_equal(st.slots.cpu().numpy(), ref.slots)
+    ref.check_pools(w)
+    ref.check_whole_pools(w)
+    assert max_abs(st.out, ref.decode()) <= TOL[w.dtype]
+    assert_no_device_error(P)
+
+
 # ------------------------------------------------------------------ shared-prefix (cascade) decode
 
 def test_cascade_step_is_deterministic(P):
