@@ -50,6 +50,15 @@ MUTANTS = [
      "            if (refcount[b] > 99) {\n                int32_t nb = take_free"),
     ("freed blocks never return to the stack",
      "if (refcount[b] == 0) free_ids[(*free_count)++] = b;", "(void)0;"),
+    ("merge normaliser dropped", "            o[d] = acc / L;", "            o[d] = acc;"),
+    ("merge skips the first range",
+     "for (int32_t k = 0; k < max_parts; ++k) if (l[k] > 0.0) L += exp(m[k] - M) * l[k];",
+     "for (int32_t k = 1; k < max_parts; ++k) if (l[k] > 0.0) L += exp(m[k] - M) * l[k];"),
+    ("padding position mapped to a slot",
+     "if (p < 0) { slot_mapping[t] = -1; continue; }",
+     "if (p < -1) { slot_mapping[t] = -1; continue; }"),
+    ("fork adds no reference", "            refcount[b] += 1;", "            refcount[b] += 0;"),
+    ("free leaves the table row", "            row[j] = -1;\n", "            (void)0;\n"),
     ("q rows read head-major",
      "qd[d] = load_as_double(q, dtype, ((int64_t)s * Hq + h) * D + d);\n            if (ctx == 0)",
      "qd[d] = load_as_double(q, dtype, ((int64_t)h * num_seqs + s) * D + d);\n            if (ctx == 0)"),

@@ -533,6 +533,7 @@ def test_fork_append_copy_on_write_free_keeps_every_sequence_intact():
     check_allocator_invariants(alloc.free_ids, alloc.free_count[0], alloc.refcount, tables, new, B)
     alloc.free(B, tables, [0, 1, 2], new[:3])
     assert int(alloc.free_count[0]) == N and np.all(alloc.refcount == 0)
+    assert np.all(tables == -1)                              # freed sequences hold no blocks
 
 
 def test_last_reference_keeps_its_block():
@@ -543,6 +544,7 @@ def test_last_reference_keeps_its_block():
     alloc.allocate_for_append(k, k, B, tables, [0, 0], [20, 0])
     alloc.fork(B, tables, [[0, 1]], [20])
     alloc.free(B, tables, [1], [20])
+    assert np.all(tables[1] == -1) and np.all(tables[0, :2] >= 0)
     owned = tables[0, 1]
     assert np.all(alloc.allocate_for_append(k, k, B, tables, [20, 0], [21, 0]) == 0)
     assert tables[0, 1] == owned                            # refcount 1: written in place
