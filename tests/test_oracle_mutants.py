@@ -59,6 +59,17 @@ MUTANTS = [
      "if (p < -1) { slot_mapping[t] = -1; continue; }"),
     ("fork adds no reference", "            refcount[b] += 1;", "            refcount[b] += 0;"),
     ("free leaves the table row", "            row[j] = -1;\n", "            (void)0;\n"),
+    ("slot mapping ignores the token's sequence",
+     "int32_t s = token_seq ? token_seq[t] : t;", "int32_t s = t;"),
+    ("partition drops its last position",
+     "int32_t n = ctx - first < P ? ctx - first : P;",
+     "int32_t n = ctx - first < P ? ctx - first - 1 : P - 1;"),
+    ("partition range maximum not subtracted",
+     "for (int32_t i = 0; i < n; ++i) { x[i] = exp(x[i] - m); l += x[i]; }",
+     "for (int32_t i = 0; i < n; ++i) { x[i] = exp(x[i]); l += x[i]; }"),
+    ("block copy direction reversed",
+     "memcpy((char*)k_pool + (int64_t)dst * block_bytes, (const char*)k_pool + (int64_t)src * block_bytes,",
+     "memcpy((char*)k_pool + (int64_t)src * block_bytes, (const char*)k_pool + (int64_t)dst * block_bytes,"),
     ("q rows read head-major",
      "qd[d] = load_as_double(q, dtype, ((int64_t)s * Hq + h) * D + d);\n            if (ctx == 0)",
      "qd[d] = load_as_double(q, dtype, ((int64_t)h * num_seqs + s) * D + d);\n            if (ctx == 0)"),
