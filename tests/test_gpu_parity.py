@@ -620,6 +620,70 @@ def test_bench_step_matches_oracle_at_full_size(P, name, out_dtype):
     assert_no_device_error(P)
 
 
+@pytest.mark.parametrize("nq", [4, 8])
+def test_multi_query_append_at_full_size_matches_oracle(P, nq):
+    """bench.py --path multi's launch (the new tokens' K/V written by the causal multi-query
+    decode launch itself, the library's automatic partitions) on the full LLaMA-13B-shaped
+    batch: every sequence's slots and the pools bit-exact, every query row within 2e-3
+    (fp32 output) of the oracle's attention on the oracle-written pools."""
+    w = workloads.make("llama13b_b16", seed=0, device=DEV)
+    S, Hq, Hkv, D, B = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size
+    g = torch.Generator(device=DEV).manual_seed(17 + nq)
+    q = torch.randn((S, nq, Hq, D), generator=g, device=DEV).half()
+    kn = torch.randn((S * nq, Hkv, D), generator=g, device=DEV).half()
+    vn = torch.randn((S * nq, Hkv, D), generator=g, device=DEV).half()
+    kr, vr = host(w.k_pool).copy(), host(w.v_pool).copy()      # before the GPU step
+    mcl = w.max_context_len
+    ws_bytes = P.pkv_decode_workspace_bytes(w.k_pool, S * nq, Hq, mcl, 0)
+    ws = P.workspace_tensor(ws_bytes, DEV) if ws_bytes else None
+    out = torch.full((S, nq, Hq, D), float("nan"), dtype=torch.float32, device=DEV)
+    slots = torch.full((S, nq), -7, dtype=torch.int64, device=DEV)
+    P.pkv_paged_attention_decode_multi_append(q, w.k_pool, w.v_pool, kn, vn,
+                                              dev_i32(w.block_tables), dev_i32(w.context_lens),
+                                              w.scale, out, mcl, 0, ws, slot_mapping=slots)
+    torch.cuda.synchronize()
+    pos = (w.context_lens[:, None] - nq + np.arange(nq)[None, :]).astype(np.int32)
+    seq = np.repeat(np.arange(S, dtype=np.int32), nq)
+    ref_slots = oracle.slot_mapping(w.block_tables, pos.reshape(-1), B, token_seq=seq)
+    assert np.array_equal(slots.cpu().numpy().reshape(-1), ref_slots)
+    oracle.kv_cache_write("f16", kr, vr, host(kn), host(vn), ref_slots)
+    assert np.array_equal(host(w.k_pool), kr) and np.array_equal(host(w.v_pool), vr)
+    ref = oracle.paged_decode_multi("f16", kr, vr, host(q), w.block_tables, w.context_lens,
+                                    w.scale)
+    assert max_abs(out, ref) <= TOL["f16"]
+    assert_no_device_error(P)
+
+
+def test_swap_at_full_size_matches_oracle(P):
+    """bench.py --path swap's moves on the full LLaMA-13B-shaped batch: a seeded quarter of
+    the blocks in use out to a pinned host pool (compared bit for bit with the oracle's
+    copy of the same blocks), the device blocks overwritten, then back in."""
+    w = workloads.make("llama13b_b16", seed=0, device=DEV)
+    used = np.unique(np.concatenate([w.block_tables[s, :-(-int(c) // w.block_size)]
+                                     for s, c in enumerate(w.context_lens)]))
+    rng = np.random.default_rng(11)
+    moved = np.sort(rng.choice(used, size=len(used) // 4, replace=False)).astype(np.int32)
+    n = len(moved)
+    shape = (n,) + tuple(w.k_pool.shape[1:])
+    hk = torch.zeros(shape, dtype=w.k_pool.dtype).pin_memory()
+    hv = torch.zeros(shape, dtype=w.v_pool.dtype).pin_memory()
+    out_pairs = np.stack([moved, np.arange(n, dtype=np.int32)], 1).astype(np.int32)
+    k0, v0 = host(w.k_pool).copy(), host(w.v_pool).copy()
+    P.pkv_swap_blocks(w.k_pool, w.v_pool, hk, hv, dev_i32(out_pairs))
+    torch.cuda.synchronize()
+    rk, rv = np.zeros_like(host(hk)), np.zeros_like(host(hv))
+    oracle.swap_blocks(k0, v0, rk, rv, out_pairs)
+    assert np.array_equal(host(hk), rk) and np.array_equal(host(hv), rv)
+    idx = torch.as_tensor(moved, device=DEV).long()
+    w.k_pool[idx] = 0
+    w.v_pool[idx] = 0
+    in_pairs = np.stack([np.arange(n, dtype=np.int32), moved], 1).astype(np.int32)
+    P.pkv_swap_blocks(hk, hv, w.k_pool, w.v_pool, dev_i32(in_pairs))
+    torch.cuda.synchronize()
+    assert np.array_equal(host(w.k_pool), k0) and np.array_equal(host(w.v_pool), v0)
+    assert_no_device_error(P)
+
+
 def test_bench_step_in_shortest_last_order_matches_oracle(P):
     """bench.py --order shortest-last: the same batch with its shortest fifth last; every
     sequence's slot, write and attention still match the oracle."""
