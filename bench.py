@@ -868,7 +868,10 @@ def run_multi(args):
         {"kernel": dec_name + " (all launches of the step)", "bound": "hbm",
          "achieved": round(total / (ms * 1e-3) / 1e9, 2), "peak": peak, "unit": "GB/s",
          "frac": round(total / (ms * 1e-3) / 1e9 / peak, 4), "peak_kind": peak_kind,
-         "traffic": None, "algorithmic_bytes": total},
+         # DRAM bytes per decode launch (the step's dominant kernel) from the committed
+         # ncu record of the fused step, when there is one for this source
+         "traffic": None if args.unfused else read_traffic("multi%d_%s" % (nq, args.workload)),
+         "algorithmic_bytes": total},
         cpu,
         {"value": round(total / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
          "ms_per_step": round(e2e_ms, 5),
